@@ -1,0 +1,418 @@
+"""Benchmark: sliding-window (+ sinks) attention on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl swa|reference]
+
+One step is one bf16 prefill of the Mistral-like layer (B=1, H=32, Hkv=8,
+d=128, n=16384, w=4096, g=0) -- the headline workload, reported as useful
+TFLOP/s (4 * connections * d * B * H floating-point operations; masked or
+padded tile work is not counted).  The decode half of the metric is measured
+in the same run on the streaming-decode workload (B=32, H=32, Hkv=8, d=128,
+w=4096, g=4, pos=100000): one cache append plus one decode per step, reported
+as HBM GB/s over the algorithmic bytes (each cached K/V row read once).
+
+Timing: W warm-up steps, then K timed steps; L2 is flushed (a 256 MiB write)
+before every timed launch and each launch is bracketed by CUDA events on the
+launching stream.  Under torchrun every rank runs its own replica (weak
+scaling); rank 0 prints one JSON line with the max time over ranks.
+
+--impl reference times the CPU oracle (the only other implementation of this
+method here) on a bounded sample of query rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+PREFILL = dict(B=1, H=32, Hkv=8, n=16384, d=128, w=4096, g=0)
+DECODE = dict(B=32, H=32, Hkv=8, d=128, w=4096, g=4, pos=100000, sink_scale=4.0)
+METRIC = "SWA prefill useful TFLOP/s (% bf16 peak); decode HBM GB/s (% peak)"
+PREFILL_KERNEL_SRC = os.path.join(ROOT, "sink_sparse_attention_swa_b300", "csrc", "swa_prefill_tc.cu")
+DECODE_KERNEL_SRC = os.path.join(ROOT, "sink_sparse_attention_swa_b300", "csrc", "swa_decode.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+
+
+def pairs(n, w, g):
+    """Connections of one head (window w including the current position, plus g sinks)."""
+    total = n * (n + 1) // 2 if n <= w else w * (w + 1) // 2 + (n - w) * w
+    m = n - w
+    if m > 0:
+        total += m * (m + 1) // 2 if m <= g else g * (g + 1) // 2 + (m - g) * g
+    return total
+
+
+def prefill_flops(c):
+    return 4 * pairs(c["n"], c["w"], c["g"]) * c["d"] * c["B"] * c["H"]
+
+
+def decode_bytes(c, elem=2):
+    kv = c["B"] * c["Hkv"] * (c["w"] + c["g"]) * c["d"] * elem * 2
+    qo = c["B"] * c["H"] * c["d"] * elem * 2
+    return kv + qo
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    src="measured")
+    except Exception:
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, src="fallback")
+
+
+def src_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload, src):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel source
+    is unchanged since (the line carries the source hash); else None."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    h = src_hash(src)
+    for line in text.splitlines():
+        m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9a-f]{16})\s*\|\s*([0-9.e+]+)\s*\|", line)
+        if m and m.group(1) == kernel and m.group(2) == workload and m.group(3) == h:
+            return float(m.group(4))
+    return None
+
+
+class Clocks:
+    """Samples nvidia-smi every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_sample(min_seconds=10.0, max_seconds=30.0, seed=0):
+    """Times the fp64 oracle on sampled query rows of the prefill workload until
+    at least `min_seconds` have passed.  Returns (TFLOP/s of useful work,
+    rows, seconds, threads)."""
+    import oracle
+    from sink_sparse_attention_swa_b300 import synthetic
+
+    oracle.set_num_threads(os.cpu_count() or 1)
+    c = PREFILL
+    x = synthetic.prefill_inputs(c["B"], c["H"], c["Hkv"], c["n"], c["d"], c["w"], c["g"],
+                                 dtype="bf16", seed=seed, device="cpu")
+    K = x.K.double().numpy()
+    V = x.V.double().numpy()
+    rows_all = synthetic.sample_rows(c["B"], c["H"], c["n"], 1 << 14, seed=1).numpy()
+    done, t_total, flops = 0, 0.0, 0
+    batch = 64
+    while t_total < min_seconds and done < rows_all.shape[0]:
+        rows = rows_all[done:done + batch]
+        qr = np.stack([x.Q[b, h, i].double().numpy() for b, h, i in rows])
+        t0 = time.perf_counter()
+        oracle.prefill_rows(qr, K, V, c["H"], c["w"], c["g"], x.scale, rows)
+        t_total += time.perf_counter() - t0
+        for _, _, i in rows:
+            i = int(i)
+            flops += 4 * c["d"] * (min(i + 1, c["w"]) + min(c["g"], max(0, i - c["w"] + 1)))
+        done += rows.shape[0]
+        if t_total < min_seconds / 4:
+            batch *= 2
+        if t_total > max_seconds:
+            break
+    return flops / t_total / 1e12, done, t_total, oracle.num_threads()
+
+
+# --------------------------------------------------------------------------- GPU legs
+def time_launches(fn, steps, warmup, flush, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for k in range(steps):
+        flush.add_(1)  # evict L2 before each timed launch
+        starts[k].record(stream)
+        fn()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def run_swa(args):
+    import sink_sparse_attention_swa_b300 as swa
+    from sink_sparse_attention_swa_b300 import synthetic
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    pk = peaks()
+    c = PREFILL
+    x = synthetic.prefill_inputs(c["B"], c["H"], c["Hkv"], c["n"], c["d"], c["w"], c["g"],
+                                 dtype="bf16", seed=rank, device=dev)
+    out = torch.empty_like(x.Q)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MiB > L2
+    fn = lambda: swa.prefill(x.Q, x.K, x.V, c["w"], c["g"], x.scale, out=out, stream=stream)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        times = time_launches(fn, args.steps, args.warmup, flush, stream)
+    barrier(world)
+    ms = max_over_ranks(float(np.mean(times)), world, dev)
+    flops = prefill_flops(c)
+    value = flops * world / (ms * 1e-3) / 1e12
+    launch_ms = float(np.mean(times))
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    traffic = recorded_traffic("swa_prefill_bf16_sm103", "mistral_like_prefill", PREFILL_KERNEL_SRC)
+
+    # ---- end to end through the public API with host buffers
+    Qh = x.Q.cpu().pin_memory()
+    Kh = x.K.cpu().pin_memory()
+    Vh = x.V.cpu().pin_memory()
+    Oh = torch.empty_like(Qh).pin_memory()
+    Qd, Kd, Vd = torch.empty_like(x.Q), torch.empty_like(x.K), torch.empty_like(x.V)
+
+    def e2e_step():
+        Qd.copy_(Qh, non_blocking=True)
+        Kd.copy_(Kh, non_blocking=True)
+        Vd.copy_(Vh, non_blocking=True)
+        swa.prefill(Qd, Kd, Vd, c["w"], c["g"], x.scale, out=out, stream=stream)
+        Oh.copy_(out, non_blocking=True)
+
+    e2e_times = time_launches(e2e_step, max(2, args.steps // 2), 2, flush, stream)
+    e2e_ms = max_over_ranks(float(np.mean(e2e_times)), world, dev)
+    h2d = (Qh.numel() + Kh.numel() + Vh.numel()) * 2
+    d2h = Oh.numel() * 2
+
+    # ---- decode leg: append one token + decode, streaming-decode workload
+    dc = DECODE
+    dx = synthetic.decode_cache_inputs(dc["B"], dc["H"], dc["Hkv"], dc["d"], dc["w"], dc["g"],
+                                       dc["pos"], dtype="bf16", seed=rank,
+                                       sink_scale=dc["sink_scale"], device=dev)
+    kn, vn = synthetic.token_stream(dc["B"], dc["Hkv"], dc["d"], 1, seed=rank + 1, device=dev)
+    dout = torch.empty_like(dx.q)
+    splits = 0
+    ws_bytes = swa.decode_workspace_bytes(dc["B"], dc["H"], dc["Hkv"], dc["d"], dc["w"], dc["g"])
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    dfn_dec = lambda: swa.decode(dx.q, dx.Kc, dx.Vc, dx.pos, dc["w"], dc["g"], dx.scale, out=dout,
+                                 workspace=ws, num_splits=splits, stream=stream)
+
+    def dfn():
+        swa.cache_append(dx.Kc, dx.Vc, kn, vn, dx.pos, dc["w"], dc["g"], stream=stream)
+        dfn_dec()
+
+    dsteps = max(args.steps, 10)
+    with Clocks(local) as dclk:
+        dtimes = time_launches(dfn, dsteps, args.warmup, flush, stream)
+        dec_only = time_launches(dfn_dec, dsteps, args.warmup, flush, stream)
+    dms = max_over_ranks(float(np.mean(dtimes)), world, dev)
+    dbytes = decode_bytes(dc)
+    dgbs = dbytes * world / (dms * 1e-3) / 1e9
+    dec_ms = float(np.mean(dec_only))
+    dec_traffic = recorded_traffic("swa_decode_split", "streaming_decode_sinks", DECODE_KERNEL_SRC)
+    assert swa.device_status(stream) == 0, "device status reported an error"
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tfl, rows, secs, thr = cpu_oracle_sample(args.cpu_seconds, 3 * args.cpu_seconds)
+        cpu = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"{rows} query rows of the Mistral-like prefill (uniformly sampled over "
+                         f"heads and positions), fp64, {secs:.1f} s"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "mistral_like_prefill", **c, "scale": "1/sqrt(d)",
+                   "l2": "flushed before each timed launch (256 MiB write)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "clocks": clk.summary(),
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"],
+                     "unit": "TFLOP/s", "frac": achieved / pk["bf16"], "traffic": traffic,
+                     "kernel": "swa_prefill_bf16_sm103", "peak_source": pk["src"] + " burst",
+                     "frac_of_sustained": achieved / pk["bf16_sustained"],
+                     "useful_flops_per_launch": flops},
+        "cpu_baseline": cpu,
+        "decode": {"workload": "streaming_decode_sinks", **{k: dc[k] for k in dc},
+                   "value": dgbs, "unit": "GB/s", "ms_per_step": dms,
+                   "step": "cache append (1 token) + decode",
+                   "roofline": {"bound": "hbm", "achieved": dbytes / (dec_ms * 1e-3) / 1e9,
+                                "peak": pk["hbm"], "unit": "GB/s",
+                                "frac": dbytes / (dec_ms * 1e-3) / 1e9 / pk["hbm"],
+                                "traffic": dec_traffic, "kernel": "swa_decode_split + merge",
+                                "decode_only_ms": dec_ms, "algorithmic_bytes": dbytes,
+                                "frac_of_8TBs": dbytes / (dec_ms * 1e-3) / 1e9 / 8000.0},
+                   "clocks": dclk.summary(), "gpu_launches": dsteps * 3},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(min(args.warmup, 1)):
+        cpu_oracle_sample(min(per, 2.0), min(per, 2.0) * 3)
+    vals, secs, rows_total, thr = [], 0.0, 0, 1
+    for _ in range(args.steps):
+        tfl, rows, s, thr = cpu_oracle_sample(per, 3 * per)
+        vals.append(tfl)
+        secs += s
+        rows_total += rows
+    value = float(np.mean(vals))
+    flops = prefill_flops(PREFILL)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": flops / (value * 1e12) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "mistral_like_prefill", **PREFILL, "scale": "1/sqrt(d)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                         "sample": f"{rows_total} sampled query rows over {args.steps} steps, "
+                                   f"{secs:.1f} s of fp64 CPU work; ms_per_step extrapolates "
+                                   f"to the whole layer"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="swa", choices=["swa", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_swa(args)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

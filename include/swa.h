@@ -1,0 +1,196 @@
+/*
+ * swa.h -- C ABI of libswa: causal sliding-window attention with attention
+ * sinks on NVIDIA B300 (sm_103a).
+ *
+ * The operation.  For a query at position i the keys it reads are the window
+ * i-w+1 .. i (w cells including the current one) united with the g "sink"
+ * positions 0 .. g-1, never a future key; every other key gets a score of
+ * -inf before the softmax:
+ *     O[i] = sum_j softmax_j(scale * q_i . k_j) v_j  over the allowed j.
+ * Sources: "Sliding Window and Sparse Attention, from Longformer to CSA2",
+ * sections 1 (attention, causal masking, prefill vs decode) and 2 (the window,
+ * the rolling buffer, attention sinks); "Local and Sparse Attention: Reading
+ * Fewer Token Positions", Figures 1 (window of w cells including the current
+ * one, -inf masking), 2 (a key in the window and the designated set is read
+ * once; no future key) and 4 (rolling cache).
+ *
+ * Conventions shared by every entry point.
+ *  - Layouts are row-major and contiguous:
+ *      prefill Q, O   [B][H][n][d]        K, V     [B][Hkv][n][d]
+ *      decode  q, O   [B][H][d]           Kc, Vc   [B][Hkv][w+g][d]
+ *      lse            [B][H][n] (prefill) or [B][H] (decode), fp32, natural log
+ *    The rolling cache keeps position p in ring slot p mod w (slots 0..w-1)
+ *    and, when p < g, also in sink slot w+p (slots w..w+g-1).
+ *  - Grouped-query attention: query head h reads key/value head h / (H/Hkv);
+ *    H must be a multiple of Hkv.
+ *  - d is 64 or 128.  Element type bf16 (accumulation in fp32) or fp32.
+ *  - All tensor pointers are device pointers owned by the caller, 16-byte
+ *    aligned.  The library never frees caller memory.
+ *  - Every launch is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  SWA_OK means "validated and enqueued".  A
+ *    device-side wait that runs out of time marks the library's device status
+ *    word and the kernel returns early; swa_get_device_status() reads and
+ *    clears it.
+ *  - Arguments are validated on the host before any launch; an invalid call
+ *    enqueues nothing and returns SWA_ERR_INVALID_ARG or SWA_ERR_UNSUPPORTED.
+ *  - Entry points are thread-safe; the only library state is the decode
+ *    workspace of swa_decode() and the per-device status word.
+ */
+#ifndef SWA_H
+#define SWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without pulling in the CUDA headers. */
+typedef struct CUstream_st *swa_stream_t;
+
+typedef enum {
+    SWA_OK = 0,
+    SWA_ERR_INVALID_ARG = -1,    /* null/unaligned pointer, bad size or value   */
+    SWA_ERR_UNSUPPORTED = -2,    /* valid but not built (e.g. d not 64 or 128)  */
+    SWA_ERR_CUDA = -3,           /* a CUDA runtime/driver call failed           */
+    SWA_ERR_DEVICE_TIMEOUT = -4, /* a kernel's bounded wait ran out (device)    */
+    SWA_ERR_ALLOC = -5,          /* library workspace allocation failed         */
+    SWA_ERR_WORKSPACE = -6       /* caller workspace too small                  */
+} swa_status;
+
+typedef enum { SWA_BF16 = 0, SWA_F32 = 1 } swa_dtype;
+
+/* ---------------------------------------------------------------------- */
+/* Prefill: the whole prompt at once, block-sparse over BMxBN tiles.       */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * swa_prefill -- bf16 prefill ("Sliding Window and Sparse Attention, from
+ * Longformer to CSA2", sections 1-2 and the block-sparsity note in section 4:
+ * only the key tiles that meet the band or the sink columns are computed).
+ *   Q [B][H][n][d], K, V [B][Hkv][n][d], O [B][H][n][d]: bf16, device.
+ *   n >= 1, w >= 1, g >= 0, scale > 0 and finite (applied to q.k).
+ * Runs the tcgen05/TMEM tensor-core kernel.  Returns SWA_OK or an error code.
+ */
+int swa_prefill(const void *Q, const void *K, const void *V, void *O,
+                int B, int H, int Hkv, int n, int d, int w, int g, float scale,
+                swa_stream_t stream);
+
+/*
+ * swa_prefill_ex -- as swa_prefill, with the element type chosen by `dtype`
+ * (SWA_BF16: tensor-core kernel; SWA_F32: fp32 CUDA-core kernel, same
+ * semantics) and an optional log-sum-exp output `lse` [B][H][n] fp32 (NULL to
+ * skip): lse = log(sum_j exp(scale*q.k_j)) over the allowed keys (section 6 of
+ * the same page: the log-sum-exp lets partial results be normalised jointly).
+ */
+int swa_prefill_ex(const void *Q, const void *K, const void *V, void *O, float *lse,
+                   int B, int H, int Hkv, int n, int d, int w, int g, float scale,
+                   swa_dtype dtype, swa_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Decode: one query token per sequence against the rolling cache.         */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * swa_decode -- bf16 single-token decode ("Sliding Window and Sparse
+ * Attention, from Longformer to CSA2", section 1: decode streams the cache
+ * from HBM; section 2: the rolling buffer and sinks).  The query of sequence
+ * b is at position pos[b] (device int32 [B], pos >= 0) and its own key/value
+ * must already be in the cache (swa_cache_append).  Slots whose position is
+ * not yet written (pos < w-1) and sink slots of positions still inside the
+ * window are not read.
+ *   q [B][H][d], Kcache, Vcache [B][Hkv][w+g][d], O [B][H][d]: bf16, device.
+ * Split-K over the cached keys, then a log-sum-exp merge; uses a library-owned
+ * workspace that grows on demand (cudaMalloc on first use of a size, so make
+ * the first call outside stream capture).
+ */
+int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos,
+               int B, int H, int Hkv, int d, int w, int g, float scale, void *O,
+               swa_stream_t stream);
+
+/* Bytes of workspace swa_decode_ex needs for these sizes and `num_splits`
+ * (0 = the split count the library would choose). */
+size_t swa_decode_workspace_bytes(int B, int H, int Hkv, int d, int w, int g, int num_splits);
+
+/*
+ * swa_decode_ex -- as swa_decode with the element type `dtype`, an optional
+ * lse [B][H] fp32 output (NULL to skip), an explicit split count `num_splits`
+ * (0 = automatic; 1..1024) and a caller-owned device workspace of
+ * `workspace_bytes` >= swa_decode_workspace_bytes(...) (16-byte aligned).
+ * Nothing is allocated.
+ */
+int swa_decode_ex(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos,
+                  int B, int H, int Hkv, int d, int w, int g, float scale, void *O,
+                  float *lse, swa_dtype dtype, int num_splits, void *workspace,
+                  size_t workspace_bytes, swa_stream_t stream);
+
+/*
+ * swa_cache_append -- rolling-buffer scatter ("Sliding Window and Sparse
+ * Attention, from Longformer to CSA2", section 2: position i overwrites slot
+ * i mod w; "Local and Sparse Attention: Reading Fewer Token Positions",
+ * Figure 4).  Writes T new tokens k_new, v_new [B][Hkv][T][d] of sequence b at
+ * positions pos0[b] .. pos0[b]+T-1 (pos0: device int32 [B], >= 0): position p
+ * goes to ring slot p mod w and, if p < g, also to sink slot w+p.  When T > w
+ * only the last w positions are written to the ring (earlier ones would be
+ * overwritten anyway); sink slots are written for every p < g.
+ * Kcache, Vcache [B][Hkv][w+g][d] of `dtype`, device.
+ */
+int swa_cache_append(void *Kcache, void *Vcache, const void *k_new, const void *v_new,
+                     const int32_t *pos0, int T, int B, int Hkv, int d, int w, int g,
+                     swa_dtype dtype, swa_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Host helpers (no GPU needed).                                           */
+/* ---------------------------------------------------------------------- */
+
+/* Number of (query, key) connections of one head over n positions
+ * ("Local and Sparse Attention: Reading Fewer Token Positions", Figure 1: 21
+ * for n=8, w=3; 36 for full causal).  Returns -1 on invalid input. */
+int64_t swa_count_pairs(int64_t n, int64_t w, int64_t g);
+
+/*
+ * Tile classes the prefill kernels use: for query tile qt (rows qt*BM ..) and
+ * key tile kt (columns kt*BN ..), cls[qt*n_kt + kt] = 0 skipped, 1 partial
+ * (element mask applied), 2 full, with n_qt = ceil(n/BM), n_kt = ceil(n/BN);
+ * `cap` is the number of int32 elements at `cls` (host memory).  Only rows < n
+ * exist; columns >= n are blocked.  Returns SWA_OK or SWA_ERR_INVALID_ARG.
+ */
+int swa_enumerate_tiles(int64_t n, int64_t w, int64_t g, int BM, int BN, int32_t *cls,
+                        size_t cap);
+
+/* Where the rolling cache keeps position p: *ring_slot = p mod w,
+ * *sink_slot = w+p if p < g else -1.  Returns SWA_OK or SWA_ERR_INVALID_ARG. */
+int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_slot);
+
+/* ---------------------------------------------------------------------- */
+/* Status and diagnostics.                                                  */
+/* ---------------------------------------------------------------------- */
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: SWA_OK, SWA_ERR_DEVICE_TIMEOUT, or SWA_ERR_CUDA if a CUDA call failed. */
+int swa_get_device_status(swa_stream_t stream);
+
+/* A static string naming a swa_status value. */
+const char *swa_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int swa_version(void);
+
+/*
+ * swa_selftest_umma -- diagnostic with no counterpart on the pages: checks the
+ * tensor-core operand encodings the prefill kernel relies on, on one tile.
+ *   A [128][128] bf16 (row-major), Bk [128][128] bf16 (row-major, read as
+ *   N x K), Bn [128][128] bf16 (row-major, read as K x N), device.
+ *   D1 = A . Bk^T with both operands from shared memory;
+ *   D2 = A . Bn with A staged through tensor memory and Bn N-contiguous.
+ *   D1, D2 [128][128] fp32, device.  One CTA.  Returns SWA_OK if enqueued.
+ */
+int swa_selftest_umma(const void *A, const void *Bk, const void *Bn, float *D1, float *D2,
+                      swa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_H */

@@ -1,0 +1,218 @@
+"""Causal sliding-window attention with attention sinks on B300 (sm_103a).
+
+A thin ctypes binding over ``libswa.so`` (C ABI in ``include/swa.h``).  The
+functions here only marshal arguments -- shapes, dtypes, pointers, the stream
+-- and call the library; every step of the computation runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (torch is used for device memory
+and streams only).  If the library is missing the import fails: there is no
+fallback.
+
+    prefill(q, k, v, w, g=0, scale=None, out=None, lse=None)        -> out
+    decode(q, k_cache, v_cache, pos, w, g=0, scale=None, ...)        -> out
+    cache_append(k_cache, v_cache, k_new, v_new, pos0, w, g=0)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "SwaError", "prefill", "decode", "cache_append", "decode_workspace_bytes",
+    "count_pairs", "enumerate_tiles", "cache_slot", "device_status", "selftest_umma",
+    "library_path", "lib",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.environ.get("SWA_LIBRARY", os.path.join(_PKG, "libswa.so"))
+
+STATUS = {0: "SWA_OK", -1: "SWA_ERR_INVALID_ARG", -2: "SWA_ERR_UNSUPPORTED", -3: "SWA_ERR_CUDA",
+          -4: "SWA_ERR_DEVICE_TIMEOUT", -5: "SWA_ERR_ALLOC", -6: "SWA_ERR_WORKSPACE"}
+SWA_BF16, SWA_F32 = 0, 1
+_DT = {torch.bfloat16: SWA_BF16, torch.float32: SWA_F32}
+
+# Every function the C header declares, with its ctypes signature.
+_i, _i64, _f, _p, _sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+SIGNATURES = {
+    "swa_prefill": (_i, [_p, _p, _p, _p] + [_i] * 7 + [_f, _p]),
+    "swa_prefill_ex": (_i, [_p, _p, _p, _p, _p] + [_i] * 7 + [_f, _i, _p]),
+    "swa_decode": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p]),
+    "swa_decode_workspace_bytes": (_sz, [_i] * 7),
+    "swa_decode_ex": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p, _i, _i, _p, _sz, _p]),
+    "swa_cache_append": (_i, [_p, _p, _p, _p, _p] + [_i] * 6 + [_i, _p]),
+    "swa_count_pairs": (_i64, [_i64, _i64, _i64]),
+    "swa_enumerate_tiles": (_i, [_i64, _i64, _i64, _i, _i, _p, _sz]),
+    "swa_cache_slot": (_i, [_i64, _i, _i, _p, _p]),
+    "swa_get_device_status": (_i, [_p]),
+    "swa_status_string": (ctypes.c_char_p, [_i]),
+    "swa_version": (_i, []),
+    "swa_selftest_umma": (_i, [_p, _p, _p, _p, _p, _p]),
+}
+
+
+class SwaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {status} ({STATUS.get(status, 'unknown')})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"libswa.so not found at {_LIB_PATH}; build it with "
+            "`python -m sink_sparse_attention_swa_b300.build` (no CPU fallback exists)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _check(name: str, rc: int) -> None:
+    if rc != 0:
+        raise SwaError(name, rc)
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def prefill(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None, lse=None,
+            stream=None):
+    """q [B,H,n,d], k/v [B,Hkv,n,d] (bf16 or fp32, CUDA) -> out [B,H,n,d].
+    lse: optional fp32 [B,H,n] output (natural-log log-sum-exp per row)."""
+    _need(q, "q")
+    B, H, n, d = q.shape
+    Hkv = k.shape[1]
+    _need(k, "k", q.dtype, (B, Hkv, n, d))
+    _need(v, "v", q.dtype, (B, Hkv, n, d))
+    if q.dtype not in _DT:
+        raise TypeError("q must be bfloat16 or float32")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, n))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.swa_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, n, d,
+                            int(w), int(g), scale, _DT[q.dtype], _stream(stream, q.device))
+    _check("swa_prefill_ex", rc)
+    return out
+
+
+def decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits=0) -> int:
+    return int(lib.swa_decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits))
+
+
+def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = None, out=None,
+           lse=None, num_splits: int = 0, workspace=None, stream=None):
+    """q [B,H,d]; k_cache/v_cache [B,Hkv,w+g,d]; pos int32 [B] (CUDA) -> out [B,H,d].
+    With workspace=None and lse=None and bf16 inputs this is swa_decode (library
+    workspace); otherwise swa_decode_ex with a workspace allocated here if needed."""
+    _need(q, "q")
+    B, H, d = q.shape
+    Hkv = k_cache.shape[1]
+    _need(k_cache, "k_cache", q.dtype, (B, Hkv, w + g, d))
+    _need(v_cache, "v_cache", q.dtype, (B, Hkv, w + g, d))
+    _need(pos, "pos", torch.int32, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, q.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = _stream(stream, q.device)
+    if workspace is None and lse is None and num_splits == 0 and q.dtype == torch.bfloat16:
+        rc = lib.swa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Hkv, d,
+                            int(w), int(g), scale, _ptr(out), st)
+        _check("swa_decode", rc)
+        return out
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H))
+    nbytes = decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits)
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.swa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Hkv, d,
+                           int(w), int(g), scale, _ptr(out), _ptr(lse), _DT[q.dtype],
+                           int(num_splits), _ptr(workspace), ws_bytes, st)
+    _check("swa_decode_ex", rc)
+    return out
+
+
+def cache_append(k_cache, v_cache, k_new, v_new, pos0, w: int, g: int = 0, stream=None):
+    """Write k_new/v_new [B,Hkv,T,d] at positions pos0[b] .. pos0[b]+T-1 into the
+    rolling caches [B,Hkv,w+g,d] (ring slot p mod w; sink slot w+p for p < g)."""
+    _need(k_cache, "k_cache")
+    B, Hkv, S, d = k_cache.shape
+    if S != w + g:
+        raise ValueError(f"cache has {S} slots, expected w+g = {w + g}")
+    _need(v_cache, "v_cache", k_cache.dtype, k_cache.shape)
+    T = k_new.shape[2]
+    _need(k_new, "k_new", k_cache.dtype, (B, Hkv, T, d))
+    _need(v_new, "v_new", k_cache.dtype, (B, Hkv, T, d))
+    _need(pos0, "pos0", torch.int32, (B,))
+    rc = lib.swa_cache_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos0),
+                              T, B, Hkv, d, int(w), int(g), _DT[k_cache.dtype],
+                              _stream(stream, k_cache.device))
+    _check("swa_cache_append", rc)
+
+
+def count_pairs(n: int, w: int, g: int) -> int:
+    return int(lib.swa_count_pairs(n, w, g))
+
+
+def enumerate_tiles(n: int, w: int, g: int, BM: int, BN: int):
+    """Tile classes [ceil(n/BM), ceil(n/BN)] as a torch int32 CPU tensor."""
+    nq, nk = -(-n // BM), -(-n // BN)
+    out = torch.zeros(nq, nk, dtype=torch.int32)
+    _check("swa_enumerate_tiles", lib.swa_enumerate_tiles(n, w, g, BM, BN, out.data_ptr(), out.numel()))
+    return out
+
+
+def cache_slot(p: int, w: int, g: int):
+    r, s = ctypes.c_int32(), ctypes.c_int32()
+    _check("swa_cache_slot", lib.swa_cache_slot(p, w, g, ctypes.byref(r), ctypes.byref(s)))
+    return r.value, s.value
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status code."""
+    return int(lib.swa_get_device_status(_stream(stream, None)))
+
+
+def selftest_umma(A, Bk, Bn, stream=None):
+    """Diagnostic: (A @ Bk^T, A @ Bn) computed by the tensor-core operand paths
+    the prefill kernel uses; A/Bk/Bn [128,128] bf16 CUDA."""
+    for t, nm in ((A, "A"), (Bk, "Bk"), (Bn, "Bn")):
+        _need(t, nm, torch.bfloat16, (128, 128))
+    D1 = torch.empty(128, 128, dtype=torch.float32, device=A.device)
+    D2 = torch.empty_like(D1)
+    _check("swa_selftest_umma", lib.swa_selftest_umma(_ptr(A), _ptr(Bk), _ptr(Bn), _ptr(D1),
+                                                      _ptr(D2), _stream(stream, A.device)))
+    return D1, D2

@@ -1,0 +1,211 @@
+// swa_api.cu -- the extern "C" entry points of libswa (declared in swa.h):
+// argument validation, workspace handling and dispatch to the launchers.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "swa_internal.h"
+
+namespace {
+
+using namespace swa;
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+// Common shape checks; returns SWA_OK, SWA_ERR_INVALID_ARG or SWA_ERR_UNSUPPORTED.
+int check_heads(int B, int H, int Hkv, int d, int w, int g)
+{
+    if (B < 1 || H < 1 || Hkv < 1 || w < 1 || g < 0) return SWA_ERR_INVALID_ARG;
+    if (H % Hkv != 0) return SWA_ERR_INVALID_ARG;
+    if (static_cast<long long>(w) + g > INT32_MAX) return SWA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return SWA_ERR_UNSUPPORTED;
+    return SWA_OK;
+}
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+Workspace g_ws[64];
+
+}  // namespace
+
+extern "C" {
+
+int swa_prefill_ex(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,
+                   int Hkv, int n, int d, int w, int g, float scale, swa_dtype dtype,
+                   swa_stream_t stream)
+{
+    int rc = check_heads(B, H, Hkv, d, w, g);
+    if (rc != SWA_OK) return rc;
+    if (n < 1 || n > INT32_MAX - 256 || !scale_ok(scale)) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SWA_ERR_INVALID_ARG;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H * ((n + 127) / 128) > INT32_MAX) return SWA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == SWA_BF16)
+        return launch_prefill_bf16(Q, K, V, O, lse, B, H, Hkv, n, d, w, g, scale, st);
+    if (dtype == SWA_F32)
+        return launch_prefill_f32(Q, K, V, O, lse, B, H, Hkv, n, d, w, g, scale, st);
+    return SWA_ERR_INVALID_ARG;
+}
+
+int swa_prefill(const void *Q, const void *K, const void *V, void *O, int B, int H, int Hkv, int n,
+                int d, int w, int g, float scale, swa_stream_t stream)
+{
+    return swa_prefill_ex(Q, K, V, O, nullptr, B, H, Hkv, n, d, w, g, scale, SWA_BF16, stream);
+}
+
+size_t swa_decode_workspace_bytes(int B, int H, int Hkv, int d, int w, int g, int num_splits)
+{
+    if (check_heads(B, H, Hkv, d, w, g) != SWA_OK || num_splits < 0 || num_splits > 1024) return 0;
+    const int s = num_splits == 0 ? choose_decode_splits(B, Hkv, w, g) : num_splits;
+    return decode_workspace_bytes(B, H, d, s);
+}
+
+int swa_decode_ex(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos, int B,
+                  int H, int Hkv, int d, int w, int g, float scale, void *O, float *lse,
+                  swa_dtype dtype, int num_splits, void *workspace, size_t workspace_bytes,
+                  swa_stream_t stream)
+{
+    int rc = check_heads(B, H, Hkv, d, w, g);
+    if (rc != SWA_OK) return rc;
+    const int G = H / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return SWA_ERR_UNSUPPORTED;
+    if (dtype != SWA_BF16 && dtype != SWA_F32) return SWA_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || num_splits < 0 || num_splits > 1024) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(Kcache) || !aligned16(Vcache) || !aligned16(O) ||
+        pos == nullptr || (reinterpret_cast<uintptr_t>(pos) & 3u))
+        return SWA_ERR_INVALID_ARG;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
+    const int s = num_splits == 0 ? choose_decode_splits(B, Hkv, w, g) : num_splits;
+    const size_t need = decode_workspace_bytes(B, H, d, s);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return SWA_ERR_WORKSPACE;
+    return launch_decode(q, Kcache, Vcache, pos, B, H, Hkv, d, w, g, scale, O, lse, dtype, s,
+                         workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos, int B,
+               int H, int Hkv, int d, int w, int g, float scale, void *O, swa_stream_t stream)
+{
+    int rc = check_heads(B, H, Hkv, d, w, g);
+    if (rc != SWA_OK) return rc;
+    const int s = choose_decode_splits(B, Hkv, w, g);
+    const size_t need = decode_workspace_bytes(B, H, d, s);
+    void *ws = nullptr;
+    if (need > 0) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SWA_ERR_CUDA;
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        Workspace &W = g_ws[dev];
+        if (W.bytes < need) {
+            if (W.ptr != nullptr) {
+                // the old buffer may still be read by an earlier launch
+                if (cudaDeviceSynchronize() != cudaSuccess) return SWA_ERR_CUDA;
+                cudaFree(W.ptr);
+                W.ptr = nullptr;
+                W.bytes = 0;
+            }
+            if (cudaMalloc(&W.ptr, need) != cudaSuccess) {
+                W.ptr = nullptr;
+                return SWA_ERR_ALLOC;
+            }
+            W.bytes = need;
+        }
+        ws = W.ptr;
+    }
+    return swa_decode_ex(q, Kcache, Vcache, pos, B, H, Hkv, d, w, g, scale, O, nullptr, SWA_BF16, s,
+                         ws, need, stream);
+}
+
+int swa_cache_append(void *Kcache, void *Vcache, const void *k_new, const void *v_new,
+                     const int32_t *pos0, int T, int B, int Hkv, int d, int w, int g,
+                     swa_dtype dtype, swa_stream_t stream)
+{
+    int rc = check_heads(B, Hkv, Hkv, d, w, g);
+    if (rc != SWA_OK) return rc;
+    if (T < 0 || (dtype != SWA_BF16 && dtype != SWA_F32)) return SWA_ERR_INVALID_ARG;
+    if (T == 0) return SWA_OK;
+    if (!aligned16(Kcache) || !aligned16(Vcache) || !aligned16(k_new) || !aligned16(v_new) ||
+        pos0 == nullptr || (reinterpret_cast<uintptr_t>(pos0) & 3u))
+        return SWA_ERR_INVALID_ARG;
+    return launch_cache_append(Kcache, Vcache, k_new, v_new, pos0, T, B, Hkv, d, w, g, dtype,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t swa_count_pairs(int64_t n, int64_t w, int64_t g)
+{
+    if (n < 0 || w < 1 || g < 0) return -1;
+    // window part: row i reads min(i+1, w) keys
+    int64_t total = (n <= w) ? n * (n + 1) / 2 : w * (w + 1) / 2 + (n - w) * w;
+    // sinks below the window start: row i >= w gains min(g, i-w+1)
+    const int64_t m = n - w;
+    if (m > 0) total += (m <= g) ? m * (m + 1) / 2 : g * (g + 1) / 2 + (m - g) * g;
+    return total;
+}
+
+int swa_enumerate_tiles(int64_t n, int64_t w, int64_t g, int BM, int BN, int32_t *cls, size_t cap)
+{
+    if (n < 1 || n > INT32_MAX / 2 || w < 1 || g < 0 || BM < 1 || BN < 1 || cls == nullptr)
+        return SWA_ERR_INVALID_ARG;
+    const int64_t nq = (n + BM - 1) / BM, nk = (n + BN - 1) / BN;
+    if (static_cast<uint64_t>(nq) * static_cast<uint64_t>(nk) > cap) return SWA_ERR_INVALID_ARG;
+    const int wi = static_cast<int>(w < INT32_MAX / 2 ? w : INT32_MAX / 2);
+    const int gi = static_cast<int>(g < INT32_MAX / 2 ? g : INT32_MAX / 2);
+    std::memset(cls, 0, sizeof(int32_t) * static_cast<size_t>(nq * nk));
+    for (int qt = 0; qt < nq; ++qt) {
+        const TileRange tr = tile_range(qt, static_cast<int>(n), wi, gi, BM, BN);
+        for (int j = 0; j < tr.count; ++j) {
+            const int kt = tile_kt(tr, j);
+            cls[static_cast<size_t>(qt) * nk + kt] = tile_full(tr, kt, wi, gi, BN) ? 2 : 1;
+        }
+    }
+    return SWA_OK;
+}
+
+int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_slot)
+{
+    if (p < 0 || w < 1 || g < 0 || ring_slot == nullptr || sink_slot == nullptr)
+        return SWA_ERR_INVALID_ARG;
+    *ring_slot = static_cast<int32_t>(p % w);
+    *sink_slot = (p < g) ? static_cast<int32_t>(w + p) : -1;
+    return SWA_OK;
+}
+
+int swa_get_device_status(swa_stream_t stream)
+{
+    return read_and_clear_status(reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *swa_status_string(int status)
+{
+    switch (status) {
+    case SWA_OK: return "SWA_OK";
+    case SWA_ERR_INVALID_ARG: return "SWA_ERR_INVALID_ARG";
+    case SWA_ERR_UNSUPPORTED: return "SWA_ERR_UNSUPPORTED";
+    case SWA_ERR_CUDA: return "SWA_ERR_CUDA";
+    case SWA_ERR_DEVICE_TIMEOUT: return "SWA_ERR_DEVICE_TIMEOUT";
+    case SWA_ERR_ALLOC: return "SWA_ERR_ALLOC";
+    case SWA_ERR_WORKSPACE: return "SWA_ERR_WORKSPACE";
+    default: return "SWA_ERR_UNKNOWN";
+    }
+}
+
+int swa_version(void) { return kVersion; }
+
+int swa_selftest_umma(const void *A, const void *Bk, const void *Bn, float *D1, float *D2,
+                      swa_stream_t stream)
+{
+    if (!aligned16(A) || !aligned16(Bk) || !aligned16(Bn) || !aligned16(D1) || !aligned16(D2))
+        return SWA_ERR_INVALID_ARG;
+    return launch_selftest_umma(A, Bk, Bn, D1, D2, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// swa_internal.h -- declarations shared by the translation units of libswa.
+// Not part of the public ABI (that is include/swa.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "swa.h"
+
+namespace swa {
+
+// ---------------------------------------------------------------------------
+// Block-sparse tile enumeration for prefill ("Sliding Window and Sparse
+// Attention, from Longformer to CSA2", section 1 last paragraph and section 4
+// "Block-sparse attention": skip whole key tiles that miss the band).
+//
+// For query tile qt (rows q0 .. q1, q1 the last row that exists) the key
+// tiles with at least one allowed pair are
+//   band tiles  kt_lo .. kt_hi, kt_lo = max(0, q0-w+1)/BN, kt_hi = q1/BN
+//   sink tiles  0 .. (min(g, q1+1)-1)/BN   (when g > 0)
+// visited as: the sink tiles below kt_lo first, then the band tiles, so a
+// tile in both sets is visited once.  A tile is full (no element mask) when
+// every key is causal for every row (k1 <= q0) and every key not below g is
+// inside every row's window (max(k0, g) > k1 or max(k0, g) >= q1-w+1).
+// Used by the kernels and by the host helper swa_enumerate_tiles; the tests
+// compare the latter with the oracle's brute force.
+// ---------------------------------------------------------------------------
+struct TileRange {
+    int q0, q1;   // first and last existing query row of the tile
+    int ns;       // number of sink-only key tiles (visited first: 0 .. ns-1)
+    int kt_lo;    // first band key tile
+    int count;    // total key tiles visited
+};
+
+__host__ __device__ inline TileRange tile_range(int qt, int n, int w, int g, int BM, int BN)
+{
+    TileRange r;
+    r.q0 = qt * BM;
+    r.q1 = (r.q0 + BM < n ? r.q0 + BM : n) - 1;
+    int lo = r.q0 - w + 1;
+    if (lo < 0) lo = 0;
+    r.kt_lo = lo / BN;
+    const int kt_hi = r.q1 / BN;
+    int ns = 0;
+    if (g > 0) {
+        const int last_sink = (g < r.q1 + 1 ? g : r.q1 + 1) - 1;
+        const int s_hi = last_sink / BN;
+        ns = (s_hi + 1 < r.kt_lo) ? s_hi + 1 : r.kt_lo;
+    }
+    r.ns = ns;
+    r.count = ns + (kt_hi - r.kt_lo + 1);
+    return r;
+}
+
+__host__ __device__ inline int tile_kt(const TileRange &r, int j)
+{
+    return j < r.ns ? j : r.kt_lo + (j - r.ns);
+}
+
+__host__ __device__ inline bool tile_full(const TileRange &r, int kt, int w, int g, int BN)
+{
+    const int k0 = kt * BN, k1 = k0 + BN - 1;
+    if (k1 > r.q0) return false;
+    const int a = k0 > g ? k0 : g;
+    return a > k1 || a >= r.q1 - w + 1;
+}
+
+// ---------------------------------------------------------------------------
+// Device status word (one per device, in swa_status.cu).  Kernels OR an error
+// code into it when a bounded wait runs out.
+// ---------------------------------------------------------------------------
+enum : int { DEV_ERR_TIMEOUT = 1, DEV_ERR_BAD_POS = 2 };
+
+int *status_ptr();          // device address of the current device's status word
+int read_and_clear_status(cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Launchers (each validates nothing: the public entry points do that).
+// ---------------------------------------------------------------------------
+int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
+                        int B, int H, int Hkv, int n, int d, int w, int g, float scale,
+                        cudaStream_t stream);
+int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
+                       int B, int H, int Hkv, int n, int d, int w, int g, float scale,
+                       cudaStream_t stream);
+int choose_decode_splits(int B, int Hkv, int w, int g);
+size_t decode_workspace_bytes(int B, int H, int d, int splits);
+int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *pos, int B,
+                  int H, int Hkv, int d, int w, int g, float scale, void *O, float *lse,
+                  swa_dtype dt, int splits, void *ws, cudaStream_t stream);
+int launch_cache_append(void *Kc, void *Vc, const void *kn, const void *vn, const int32_t *pos0,
+                        int T, int B, int Hkv, int d, int w, int g, swa_dtype dt,
+                        cudaStream_t stream);
+int launch_selftest_umma(const void *A, const void *Bk, const void *Bn, float *D1, float *D2,
+                         cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace swa

@@ -1,0 +1,119 @@
+// swa_prefill_simt.cu -- fp32 sliding-window (+ sinks) prefill on the CUDA
+// cores.  Same semantics and the same block-sparse tile walk as the bf16
+// tensor-core kernel, fp32 end to end, for inputs that must keep fp32
+// precision (tensor-core TF32/BF16 cannot meet a 1e-5 error bound).
+//
+// ("Sliding Window and Sparse Attention, from Longformer to CSA2", sections
+// 1-2; "Local and Sparse Attention: Reading Fewer Token Positions", Figures
+// 1-2.)  One CTA per (q tile of 64 rows, head, batch); one query row per
+// thread; key/value tiles of 32 rows staged in shared memory; online softmax
+// in base 2 with the scale folded in.
+#include <cmath>
+
+#include "swa_internal.h"
+
+namespace swa {
+namespace {
+
+constexpr int TM = 64;
+constexpr int TN = 32;
+
+template <int HD>
+__global__ void __launch_bounds__(TM)
+    swa_prefill_f32_simt(const float *__restrict__ Q, const float *__restrict__ K,
+                         const float *__restrict__ V, float *__restrict__ O,
+                         float *__restrict__ lse, int H, int Hkv, int n, int w, int g, float sl2)
+{
+    __shared__ __align__(16) float sK[TN][HD];
+    __shared__ __align__(16) float sV[TN][HD];
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int kvh = h / (H / Hkv);
+    const int r = threadIdx.x;
+    const int i = qt * TM + r;
+    const size_t qrow = (static_cast<size_t>(b) * H + h) * n + i;
+    const float *Kb = K + (static_cast<size_t>(b) * Hkv + kvh) * n * HD;
+    const float *Vb = V + (static_cast<size_t>(b) * Hkv + kvh) * n * HD;
+
+    float q[HD], acc[HD];
+#pragma unroll
+    for (int e = 0; e < HD; ++e) {
+        q[e] = (i < n) ? Q[qrow * HD + e] : 0.f;
+        acc[e] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    const TileRange tr = tile_range(qt, n, w, g, TM, TN);
+    const int lo = i - w + 1;
+    for (int j = 0; j < tr.count; ++j) {
+        const int k0 = tile_kt(tr, j) * TN;
+        __syncthreads();
+        for (int x = r; x < TN * HD / 4; x += TM) {
+            const int row = x / (HD / 4), c4 = x % (HD / 4);
+            const int kk = k0 + row;
+            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+            if (kk < n) {
+                kv = reinterpret_cast<const float4 *>(Kb + static_cast<size_t>(kk) * HD)[c4];
+                vv = reinterpret_cast<const float4 *>(Vb + static_cast<size_t>(kk) * HD)[c4];
+            }
+            reinterpret_cast<float4 *>(&sK[row][0])[c4] = kv;
+            reinterpret_cast<float4 *>(&sV[row][0])[c4] = vv;
+        }
+        __syncthreads();
+        float s[TN];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const int jj = k0 + c;
+            const bool allowed = (i < n) && (jj <= i) && (jj >= lo || jj < g);
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < HD; ++e) dot = fmaf(q[e], sK[c][e], dot);
+            s[c] = allowed ? dot * sl2 : -INFINITY;
+            mt = fmaxf(mt, s[c]);
+        }
+        if (mt == -INFINITY) continue;  // no allowed key for this row in the tile
+        const float m_new = fmaxf(m, mt);
+        const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
+        l *= alpha;
+#pragma unroll
+        for (int e = 0; e < HD; ++e) acc[e] *= alpha;
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const float pc = exp2f(s[c] - m_new);
+            l += pc;
+#pragma unroll
+            for (int e = 0; e < HD; ++e) acc[e] = fmaf(pc, sV[c][e], acc[e]);
+        }
+        m = m_new;
+    }
+    if (i < n) {
+        const float inv = 1.f / l;
+#pragma unroll
+        for (int e = 0; e < HD; ++e) O[qrow * HD + e] = acc[e] * inv;
+        if (lse != nullptr) lse[qrow] = (m + log2f(l)) * 0.69314718055994530942f;
+    }
+}
+
+template <int HD>
+int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,
+              int Hkv, int n, int w, int g, float scale, cudaStream_t stream)
+{
+    dim3 grid((n + TM - 1) / TM, H, B);
+    swa_prefill_f32_simt<HD><<<grid, TM, 0, stream>>>(
+        static_cast<const float *>(Q), static_cast<const float *>(K),
+        static_cast<const float *>(V), static_cast<float *>(O), lse, H, Hkv, n, w, g,
+        scale * 1.4426950408889634f);
+    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                       int H, int Hkv, int n, int d, int w, int g, float scale,
+                       cudaStream_t stream)
+{
+    if (d == 64) return launch_hd<64>(Q, K, V, O, lse, B, H, Hkv, n, w, g, scale, stream);
+    if (d == 128) return launch_hd<128>(Q, K, V, O, lse, B, H, Hkv, n, w, g, scale, stream);
+    return SWA_ERR_UNSUPPORTED;
+}
+
+}  // namespace swa

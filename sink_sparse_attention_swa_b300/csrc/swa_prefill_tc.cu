@@ -1,0 +1,684 @@
+// swa_prefill_tc.cu -- bf16 block-sparse sliding-window (+ sinks) prefill on
+// the sm_103a tensor cores.
+//
+// What it computes ("Sliding Window and Sparse Attention, from Longformer to
+// CSA2", sections 1-2; "Local and Sparse Attention: Reading Fewer Token
+// Positions", Figures 1-2): O = softmax(scale * Q K^T + mask) V per head, the
+// mask -inf outside {i-w+1 .. i} u {0 .. g-1} n {j <= i}.  Exact: the
+// FlashAttention-style tiling and online softmax change the order of the
+// arithmetic, not the result ("Sparse Attention ..." social post, section 2;
+// the walkthrough's section 1 last paragraph).
+//
+// Design (B300-native; the pages give no kernel):
+//  * Persistent CTAs, one per SM.  A work item is (b, kv head, q tile of 128
+//    rows, query head of the group); items of one kv head are adjacent so the
+//    K/V band stays in L2 across the CTAs that run them together.
+//  * Only key tiles (128 keys) that meet the band or the sink columns are
+//    visited (tile_range); the element mask is applied only on partial tiles.
+//  * Warp roles (192 threads):
+//      warp 0  TMA producer: Q tile (double-buffered), K and V tiles into a
+//              2-stage ring, 128-byte swizzled boxes of 64 columns.
+//      warp 1  MMA issuer: S = Q K^T (both operands from shared memory) into
+//              one of two TMEM S buffers; O += P V with P read from TMEM and V
+//              N-major from shared memory.  tcgen05.commit signals mbarriers.
+//      warps 2-5  softmax: one query row per thread (its TMEM lane), fp32
+//              online softmax in base 2 with the scale folded in, lazy O
+//              rescaling (only when a row max grows by more than 2^8), P to
+//              TMEM as bf16, then the epilogue O / l -> bf16 and the LSE.
+//  * TMEM (512 columns): O [0, d), S0 [128, 256), S1 [256, 384),
+//    P0 [384, 448), P1 [448, 512).
+//  * Every mbarrier wait is bounded (mbar_wait): on a timeout the CTA marks
+//    the device status word, all roles stop, in-flight TMA loads and MMAs are
+//    drained with bounded waits, and TMEM is freed before exit.
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "swa_internal.h"
+#include "swa_ptx.cuh"
+
+namespace swa {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int STAGES = 2;
+constexpr int NTHREADS = 192;
+constexpr uint64_t TIMEOUT_NS = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL0 = 128;
+constexpr uint32_t P_COL0 = 384;
+constexpr float RESCALE_LOG2 = 8.0f;
+
+template <int HD>
+struct Layout {
+    static constexpr uint32_t QB = BM * HD * 2;    // one Q tile
+    static constexpr uint32_t KB = BN * HD * 2;    // one K (or V) tile
+    static constexpr uint32_t Q_OFF = 0;           // 2 Q buffers
+    static constexpr uint32_t K_OFF = Q_OFF + 2 * QB;
+    static constexpr uint32_t V_OFF = K_OFF + STAGES * KB;
+    static constexpr uint32_t BAR_OFF = V_OFF + STAGES * KB;
+    enum {
+        Q_FULL = 0,
+        Q_EMPTY = 2,
+        K_FULL = 4,
+        V_FULL = K_FULL + STAGES,
+        KV_EMPTY = V_FULL + STAGES,
+        S_FULL = KV_EMPTY + STAGES,
+        S_EMPTY = S_FULL + 2,
+        P_FULL = S_EMPTY + 2,
+        PV_DONE = P_FULL + 2,
+        O_EMPTY = PV_DONE + 2,
+        DRAIN = O_EMPTY + 1,
+        NBAR = DRAIN + 1
+    };
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t BYTES = MISC_OFF + 16;
+    // > half of the SM's shared memory, so that exactly one CTA (and one
+    // 512-column TMEM allocation) lives on an SM.
+    static constexpr uint32_t DYN_SMEM = (BYTES + 1024 > 120 * 1024) ? BYTES + 1024 : 120 * 1024;
+};
+
+struct PrefillParams {
+    int B, H, Hkv, n, w, g, G, n_qt, num_items;
+    float sl2;  // scale * log2(e)
+    __nv_bfloat16 *O;
+    float *lse;
+    int *status;
+};
+
+__device__ __forceinline__ void decode_item(int t, const PrefillParams &p, int &b, int &h, int &kvh,
+                                            int &qt)
+{
+    const int hg = t % p.G;
+    t /= p.G;
+    qt = t % p.n_qt;
+    t /= p.n_qt;
+    kvh = t % p.Hkv;
+    b = t / p.Hkv;
+    h = kvh * p.G + hg;
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// All 32 lanes wait; the outcome is made warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          int *status)
+{
+    const bool ok = mbar_wait(bar, parity, abort, status, TIMEOUT_NS);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    swa_prefill_bf16_sm103(const __grid_constant__ CUtensorMap tmQ,
+                           const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const PrefillParams p)
+{
+    using L = Layout<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t sQ = sb + L::Q_OFF, sK = sb + L::K_OFF, sV = sb + L::V_OFF;
+    const uint32_t bars = sb + L::BAR_OFF;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#define BAR(i) (bars + 8u * static_cast<uint32_t>(i))
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(BAR(L::Q_FULL + i), 1);
+            mbar_init(BAR(L::Q_EMPTY + i), 1);
+            mbar_init(BAR(L::S_FULL + i), 1);
+            mbar_init(BAR(L::S_EMPTY + i), 4);
+            mbar_init(BAR(L::P_FULL + i), 4);
+            mbar_init(BAR(L::PV_DONE + i), 1);
+        }
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(BAR(L::K_FULL + i), 1);
+            mbar_init(BAR(L::V_FULL + i), 1);
+            mbar_init(BAR(L::KV_EMPTY + i), 1);
+        }
+        mbar_init(BAR(L::O_EMPTY), 4);
+        mbar_init(BAR(L::DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch(&tmQ);
+        tma_prefetch(&tmK);
+        tma_prefetch(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int kv_iter = 0, it = 0;
+            int last_k_par[STAGES], last_q_par[2];
+            for (int s = 0; s < STAGES; ++s) last_k_par[s] = -1;
+            last_q_par[0] = last_q_par[1] = -1;
+            bool ok = true;
+            auto load_q = [&](int item, int idx) -> bool {
+                int b, h, kvh, qt;
+                decode_item(item, p, b, h, kvh, qt);
+                const int qb = idx & 1;
+                if (!mbar_wait(BAR(L::Q_EMPTY + qb), ((idx >> 1) & 1) ^ 1, abort_flag, p.status,
+                               TIMEOUT_NS))
+                    return false;
+                mbar_expect_tx(BAR(L::Q_FULL + qb), L::QB);
+                for (int c = 0; c < HD / 64; ++c)
+                    tma_load_3d(sQ + qb * L::QB + c * (BM * 128), &tmQ, BAR(L::Q_FULL + qb), c * 64,
+                                qt * BM, b * p.H + h);
+                last_q_par[qb] = (idx >> 1) & 1;
+                return true;
+            };
+            if (static_cast<int>(blockIdx.x) < p.num_items) ok = load_q(blockIdx.x, 0);
+            for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
+                int b, h, kvh, qt;
+                decode_item(t, p, b, h, kvh, qt);
+                const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+                for (int j = 0; j < tr.count; ++j, ++kv_iter) {
+                    const int st = kv_iter % STAGES;
+                    const uint32_t ph = (kv_iter / STAGES) & 1;
+                    if (!mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status,
+                                   TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    const int k0 = tile_kt(tr, j) * BN;
+                    const int zkv = b * p.Hkv + kvh;
+                    mbar_expect_tx(BAR(L::K_FULL + st), L::KB);
+                    for (int c = 0; c < HD / 64; ++c)
+                        tma_load_3d(sK + st * L::KB + c * (BN * 128), &tmK, BAR(L::K_FULL + st),
+                                    c * 64, k0, zkv);
+                    mbar_expect_tx(BAR(L::V_FULL + st), L::KB);
+                    for (int c = 0; c < HD / 64; ++c)
+                        tma_load_3d(sV + st * L::KB + c * (BN * 128), &tmV, BAR(L::V_FULL + st),
+                                    c * 64, k0, zkv);
+                    last_k_par[st] = static_cast<int>(ph);
+                    if (j == 0 && t + static_cast<int>(gridDim.x) < p.num_items) {
+                        // prefetch the next item's Q one item ahead
+                        if (!load_q(t + gridDim.x, it + 1)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                // drain: wait (bounded, ignoring the abort flag) for every load
+                // still in flight to land before the CTA may exit
+                for (int s = 0; s < STAGES; ++s)
+                    if (last_k_par[s] >= 0) {
+                        mbar_wait(BAR(L::K_FULL + s), last_k_par[s], nullptr, nullptr, TIMEOUT_NS);
+                        mbar_wait(BAR(L::V_FULL + s), last_k_par[s], nullptr, nullptr, TIMEOUT_NS);
+                    }
+                for (int q = 0; q < 2; ++q)
+                    if (last_q_par[q] >= 0)
+                        mbar_wait(BAR(L::Q_FULL + q), last_q_par[q], nullptr, nullptr, TIMEOUT_NS);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(128, BN, 0);
+            const uint32_t idesc_o = idesc_bf16_f32(128, HD, 1);
+            int kv_iter = 0, it = 0, c = 0;
+            bool ok = true;
+            // the PV product of the previous tile, issued after the next S
+            bool have_prev = false;
+            int prev_st = 0, prev_c = 0, prev_it = 0;
+            uint32_t prev_ph = 0;
+            bool prev_first = false;
+            auto issue_pv = [&]() -> bool {
+                const int pb = prev_c & 1;
+                if (!mbar_wait(BAR(L::P_FULL + pb), (prev_c >> 1) & 1, abort_flag, p.status,
+                               TIMEOUT_NS))
+                    return false;
+                if (!mbar_wait(BAR(L::V_FULL + prev_st), prev_ph, abort_flag, p.status, TIMEOUT_NS))
+                    return false;
+                if (prev_first && !mbar_wait(BAR(L::O_EMPTY), (prev_it & 1) ^ 1, abort_flag,
+                                             p.status, TIMEOUT_NS))
+                    return false;
+                tc_fence_after();
+                const uint32_t vbase = sV + prev_st * L::KB;
+                for (int ks = 0; ks < BN / 16; ++ks) {
+                    const uint64_t bdesc = smem_desc_sw128(vbase + ks * (16 * 128), BN * 128, 1024);
+                    mma_ts(tmem, tmem + P_COL0 + pb * (BN / 2) + ks * 8, bdesc, idesc_o,
+                           (!prev_first || ks > 0) ? 1u : 0u);
+                }
+                tc_commit(BAR(L::KV_EMPTY + prev_st));
+                tc_commit(BAR(L::PV_DONE + pb));
+                return true;
+            };
+            for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
+                int b, h, kvh, qt;
+                decode_item(t, p, b, h, kvh, qt);
+                const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+                const int qb = it & 1;
+                if (!mbar_wait(BAR(L::Q_FULL + qb), (it >> 1) & 1, abort_flag, p.status,
+                               TIMEOUT_NS)) {
+                    ok = false;
+                    break;
+                }
+                for (int j = 0; j < tr.count; ++j, ++kv_iter, ++c) {
+                    const int st = kv_iter % STAGES;
+                    const uint32_t ph = (kv_iter / STAGES) & 1;
+                    const int sbuf = c & 1;
+                    if (!mbar_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, TIMEOUT_NS) ||
+                        !mbar_wait(BAR(L::S_EMPTY + sbuf), ((c >> 1) & 1) ^ 1, abort_flag, p.status,
+                                   TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t qbase = sQ + qb * L::QB, kbase = sK + st * L::KB;
+                    for (int ks = 0; ks < HD / 16; ++ks) {
+                        const uint32_t blk = ks >> 2, sub = ks & 3;
+                        const uint64_t adesc =
+                            smem_desc_sw128(qbase + blk * (BM * 128) + sub * 32, 16, 1024);
+                        const uint64_t bdesc =
+                            smem_desc_sw128(kbase + blk * (BN * 128) + sub * 32, 16, 1024);
+                        mma_ss(tmem + S_COL0 + sbuf * BN, adesc, bdesc, idesc_s, ks > 0 ? 1u : 0u);
+                    }
+                    tc_commit(BAR(L::S_FULL + sbuf));
+                    if (j == tr.count - 1) tc_commit(BAR(L::Q_EMPTY + qb));
+                    if (have_prev && !issue_pv()) {
+                        ok = false;
+                        break;
+                    }
+                    have_prev = true;
+                    prev_st = st;
+                    prev_ph = ph;
+                    prev_c = c;
+                    prev_it = it;
+                    prev_first = (j == 0);
+                }
+            }
+            if (ok && have_prev) issue_pv();
+            // drain: every MMA this thread issued has completed before exit
+            tc_commit(BAR(L::DRAIN));
+            mbar_wait(BAR(L::DRAIN), 0, nullptr, nullptr, TIMEOUT_NS);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int sub = warp & 3;                 // TMEM lane quarter this warp may access
+        const int r = sub * 32 + lane;            // query row within the tile
+        const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
+        const float sl2 = p.sl2;
+        int c = 0, it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
+            int b, h, kvh, qt;
+            decode_item(t, p, b, h, kvh, qt);
+            const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+            const int i = tr.q0 + r;
+            const int lo = i - p.w + 1;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < tr.count; ++j, ++c) {
+                const int sbuf = c & 1;
+                if (!warp_wait(BAR(L::S_FULL + sbuf), (c >> 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t s[4][32];
+                const uint32_t sa = tmem + lane_off + S_COL0 + sbuf * BN;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_ld32(sa + q * 32, s[q]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) reg_fence32(s[q]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(L::S_EMPTY + sbuf));
+
+                const int kt = tile_kt(tr, j);
+                const int k0 = kt * BN;
+                if (!tile_full(tr, kt, p.w, p.g, BN)) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int jj = k0 + q * 32 + e;
+                            const bool allowed = (jj <= i) && (jj >= lo || jj < p.g);
+                            if (!allowed) s[q][e] = __float_as_uint(-INFINITY);
+                        }
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    mx0 = fmaxf(mx0, __uint_as_float(s[0][e]));
+                    mx1 = fmaxf(mx1, __uint_as_float(s[1][e]));
+                    mx2 = fmaxf(mx2, __uint_as_float(s[2][e]));
+                    mx3 = fmaxf(mx3, __uint_as_float(s[3][e]));
+                }
+                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const float m_new = fmaxf(m, m_tile);
+                if (j == 0) {
+                    m = m_new;  // O is overwritten by this item's first P V product
+                } else {
+                    const bool need = m_new > m + RESCALE_LOG2;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float alpha = need ? ex2(m - m_new) : 1.f;
+                        if (need) m = m_new;
+                        l *= alpha;
+                        // O must be complete: wait for the previous tile's P V
+                        const int pc = c - 1;
+                        if (!warp_wait(BAR(L::PV_DONE + (pc & 1)), (pc >> 1) & 1, abort_flag,
+                                       p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int q = 0; q < HD / 32; ++q) {
+                            uint32_t o[32];
+                            tmem_ld32(tmem + lane_off + q * 32, o);
+                            tmem_ld_wait();
+                            reg_fence32(o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tmem + lane_off + q * 32, o);
+                        }
+                        tmem_st_wait();
+                    }
+                }
+                const float m_use = (m == -INFINITY) ? 0.f : m;
+                uint32_t pk[2][32];
+                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float p0 = ex2(fmaf(__uint_as_float(s[q][e]), sl2, -m_use));
+                        const float p1 = ex2(fmaf(__uint_as_float(s[q][e + 1]), sl2, -m_use));
+                        if (e & 2) {
+                            l2 += p0;
+                            l3 += p1;
+                        } else {
+                            l0 += p0;
+                            l1 += p1;
+                        }
+                        pk[q >> 1][(q & 1) * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+                    }
+                l += (l0 + l1) + (l2 + l3);
+                // P buffer (c & 1) is free once the P V of tile c-2 has completed
+                if (c >= 2 && !warp_wait(BAR(L::PV_DONE + (c & 1)), ((c >> 1) & 1) ^ 1, abort_flag,
+                                         p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t pa = tmem + lane_off + P_COL0 + (c & 1) * (BN / 2);
+                tmem_st32(pa, pk[0]);
+                tmem_st32(pa + 32, pk[1]);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(L::P_FULL + (c & 1)));
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- epilogue
+            const int pc = c - 1;
+            if (!warp_wait(BAR(L::PV_DONE + (pc & 1)), (pc >> 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + i) * HD;
+#pragma unroll 1
+            for (int q = 0; q < HD / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + q * 32, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                uint32_t pkd[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pkd[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
+                                         __uint_as_float(o[2 * e + 1]) * inv_l);
+                if (i < p.n) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(L::O_EMPTY));
+            if (p.lse != nullptr && i < p.n)
+                p.lse[static_cast<size_t>(b * p.H + h) * p.n + i] =
+                    (m + log2f(l)) * 0.69314718055994530942f;
+        }
+    }
+#undef BAR
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------------
+// One-tile self-test of the operand encodings (no counterpart on the pages).
+// ------------------------------------------------------------------------
+__global__ void __launch_bounds__(128, 1)
+    swa_selftest_umma_sm103(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmBk,
+                            const __grid_constant__ CUtensorMap tmBn, const __nv_bfloat16 *A,
+                            float *D1, float *D2, int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t sA = sb, sBk = sb + 32768, sBn = sb + 65536;
+    const uint32_t bar_ld = sb + 98304, bar_mma = bar_ld + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + 98304 + 16);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        mbar_expect_tx(bar_ld, 3 * 32768);
+        for (int c = 0; c < 2; ++c) {
+            tma_load_3d(sA + c * 16384, &tmA, bar_ld, c * 64, 0, 0);
+            tma_load_3d(sBk + c * 16384, &tmBk, bar_ld, c * 64, 0, 0);
+            tma_load_3d(sBn + c * 16384, &tmBn, bar_ld, c * 64, 0, 0);
+        }
+        ok = mbar_wait(bar_ld, 0, nullptr, status, TIMEOUT_NS);
+    }
+    // A into TMEM columns 256..319 as bf16 pairs, one row per thread
+    {
+        const int r = threadIdx.x;
+        const uint32_t *arow = reinterpret_cast<const uint32_t *>(A + r * 128);
+        uint32_t v[2][32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            v[0][e] = arow[e];
+            v[1][e] = arow[32 + e];
+        }
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        tmem_st32(tmem + lane_off + 256, v[0]);
+        tmem_st32(tmem + lane_off + 288, v[1]);
+        tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0 && ok) {
+        const uint32_t id1 = idesc_bf16_f32(128, 128, 0);
+        const uint32_t id2 = idesc_bf16_f32(128, 128, 1);
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t blk = ks >> 2, sub = ks & 3;
+            mma_ss(tmem + 0, smem_desc_sw128(sA + blk * 16384 + sub * 32, 16, 1024),
+                   smem_desc_sw128(sBk + blk * 16384 + sub * 32, 16, 1024), id1, ks > 0);
+        }
+        for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tmem + 128, tmem + 256 + ks * 8, smem_desc_sw128(sBn + ks * 2048, 16384, 1024),
+                   id2, ks > 0);
+        tc_commit(bar_mma);
+        mbar_wait(bar_mma, 0, nullptr, status, TIMEOUT_NS);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    {
+        const int r = threadIdx.x;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        for (int q = 0; q < 4; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + q * 32, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+            for (int e = 0; e < 32; ++e) D1[r * 128 + q * 32 + e] = __uint_as_float(o[e]);
+            tmem_ld32(tmem + lane_off + 128 + q * 32, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+            for (int e = 0; e < 32; ++e) D2[r * 128 + q * 32 + e] = __uint_as_float(o[e]);
+        }
+    }
+    (void)lane;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------------
+// Host side: tensor maps and launches.
+// ------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// bf16 tensor [d2][d1][d0] (d0 contiguous) tiled in boxes of {64, rows, 1},
+// 128-byte swizzle, zero fill outside the tensor.
+bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint32_t rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {64, rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HD>
+int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,
+              int Hkv, int n, int w, int g, float scale, cudaStream_t stream)
+{
+    using L = Layout<HD>;
+    CUtensorMap mq, mk, mv;
+    if (!make_map_3d(&mq, Q, HD, n, static_cast<uint64_t>(B) * H, BM) ||
+        !make_map_3d(&mk, K, HD, n, static_cast<uint64_t>(B) * Hkv, BN) ||
+        !make_map_3d(&mv, V, HD, n, static_cast<uint64_t>(B) * Hkv, BN))
+        return SWA_ERR_CUDA;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(swa_prefill_bf16_sm103<HD>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
+    });
+    if (attr_err != cudaSuccess) return SWA_ERR_CUDA;
+    PrefillParams p;
+    p.B = B;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.n = n;
+    p.w = w;
+    p.g = g;
+    p.G = H / Hkv;
+    p.n_qt = (n + BM - 1) / BM;
+    p.num_items = B * H * p.n_qt;
+    p.sl2 = scale * 1.4426950408889634f;
+    p.O = static_cast<__nv_bfloat16 *>(O);
+    p.lse = lse;
+    p.status = status_ptr();
+    if (p.status == nullptr) return SWA_ERR_CUDA;
+    const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
+    swa_prefill_bf16_sm103<HD><<<grid, NTHREADS, L::DYN_SMEM, stream>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                        int H, int Hkv, int n, int d, int w, int g, float scale,
+                        cudaStream_t stream)
+{
+    if (d == 128) return launch_hd<128>(Q, K, V, O, lse, B, H, Hkv, n, w, g, scale, stream);
+    if (d == 64) return launch_hd<64>(Q, K, V, O, lse, B, H, Hkv, n, w, g, scale, stream);
+    return SWA_ERR_UNSUPPORTED;
+}
+
+int launch_selftest_umma(const void *A, const void *Bk, const void *Bn, float *D1, float *D2,
+                         cudaStream_t stream)
+{
+    CUtensorMap ma, mbk, mbn;
+    if (!make_map_3d(&ma, A, 128, 128, 1, 128) || !make_map_3d(&mbk, Bk, 128, 128, 1, 128) ||
+        !make_map_3d(&mbn, Bn, 128, 128, 1, 128))
+        return SWA_ERR_CUDA;
+    const int smem = 98304 + 64 + 1024;
+    if (cudaFuncSetAttribute(swa_selftest_umma_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    int *st = status_ptr();
+    if (st == nullptr) return SWA_ERR_CUDA;
+    swa_selftest_umma_sm103<<<1, 128, smem, stream>>>(
+        ma, mbk, mbn, static_cast<const __nv_bfloat16 *>(A), D1, D2, st);
+    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+}  // namespace swa

@@ -10,7 +10,27 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
-    config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+def _build_library():
+    from sink_sparse_attention_swa_b300 import build as b
+
+    return b.build()
+
+
+# The C-ABI library is built in-tree before any test imports the package.
+_build_library()
+
+
+def pytest_collection_modifyitems(config, items):
+    import torch
+
+    if torch.cuda.is_available():
+        return
+    skip = pytest.mark.skip(reason="no CUDA device")
+    for it in items:
+        if "gpu" in it.keywords:
+            it.add_marker(skip)
 
 
 @pytest.fixture(scope="session")
@@ -19,3 +39,10 @@ def oracle_mod():
 
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def swa():
+    import sink_sparse_attention_swa_b300 as m
+
+    return m

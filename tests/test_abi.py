@@ -1,0 +1,115 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every symbol
+the header declares, validates arguments on the host, and its host helpers
+(connection counts, tile classes, cache slots) agree bit-exactly with the
+oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "swa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("swa_prefill", "swa_decode", "swa_cache_append"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(swa):
+    lib = ctypes.CDLL(swa.library_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(swa.SIGNATURES)
+
+
+def test_version_and_status_strings(swa):
+    assert swa.lib.swa_version() >= 100
+    for code, name in swa.STATUS.items():
+        assert swa.lib.swa_status_string(code).decode() == name
+
+
+def test_count_pairs_matches_oracle(swa, oracle_mod):
+    for n in (1, 2, 7, 8, 9, 63, 64, 65, 300):
+        for w in (1, 2, 3, 8, 64, 500):
+            for g in (0, 1, 4, 9):
+                assert swa.count_pairs(n, w, g) == oracle_mod.count_pairs(n, w, g), (n, w, g)
+    assert swa.count_pairs(8, 3, 0) == 21 and swa.count_pairs(8, 8, 0) == 36
+    assert swa.count_pairs(16384, 4096, 0) == oracle_mod.count_pairs(16384, 4096, 0)
+    assert swa.count_pairs(131072, 4096, 4) == 528992250
+    assert swa.count_pairs(-1, 3, 0) == -1
+
+
+@pytest.mark.parametrize("BM,BN", [(128, 128), (64, 32), (16, 16), (128, 64), (32, 128)])
+def test_tile_classes_match_oracle(swa, oracle_mod, BM, BN):
+    rng = np.random.default_rng(BM * 1000 + BN)
+    cases = [(1, 1, 0), (300, 64, 0), (300, 100, 4), (257, 3, 1), (200, 1000, 0), (129, 128, 130),
+             (333, 17, 5), (1000, 129, 1), (512, 64, 0), (700, 256, 300)]
+    cases += [(int(rng.integers(1, 700)), int(rng.integers(1, 400)), int(rng.integers(0, 20)))
+              for _ in range(12)]
+    for n, w, g in cases:
+        mine = swa.enumerate_tiles(n, w, g, BM, BN).numpy()
+        ref = oracle_mod.tiles(n, w, g, BM, BN)
+        assert np.array_equal(mine, ref), (n, w, g, BM, BN)
+
+
+def test_tile_classes_workload_counts(swa):
+    # partial/full tile counts per head at 128x128 tiles for the benchmark shapes
+    t = swa.enumerate_tiles(16384, 4096, 0, 128, 128).numpy()
+    assert (t == 2).sum() == 3472 and (t == 1).sum() == 224
+    t = swa.enumerate_tiles(32768, 1024, 0, 128, 128).numpy()
+    assert (t == 2).sum() == 1764 and (t == 1).sum() == 504
+
+
+def test_cache_slot_matches_oracle(swa, oracle_mod):
+    for w, g in [(3, 0), (3, 1), (4096, 4), (8, 2), (1, 5)]:
+        for p in list(range(0, 20)) + [4095, 4096, 100000]:
+            assert swa.cache_slot(p, w, g) == oracle_mod.cache_slots(p, w, g), (p, w, g)
+    with pytest.raises(swa.SwaError):
+        swa.cache_slot(-1, 3, 0)
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
+
+
+def test_host_validation_rejects_before_launch(swa):
+    L = swa.lib
+    ok_args = dict(B=1, H=4, Hkv=2, n=16, d=128, w=4, g=0, scale=0.1)
+
+    def prefill(**kw):
+        a = dict(ok_args, **kw)
+        return L.swa_prefill_ex(FAKE, FAKE, FAKE, FAKE, None, a["B"], a["H"], a["Hkv"], a["n"],
+                                a["d"], a["w"], a["g"], a["scale"], 0, None)
+
+    assert prefill(d=96) == -2          # unsupported head size
+    assert prefill(H=3) == -1           # H not a multiple of Hkv
+    assert prefill(w=0) == -1
+    assert prefill(g=-1) == -1
+    assert prefill(n=0) == -1
+    assert prefill(scale=0.0) == -1
+    assert prefill(scale=float("nan")) == -1
+    assert L.swa_prefill_ex(FAKE + 8, FAKE, FAKE, FAKE, None, 1, 4, 2, 16, 128, 4, 0, 0.1, 0,
+                            None) == -1  # misaligned Q
+    assert L.swa_prefill_ex(None, FAKE, FAKE, FAKE, None, 1, 4, 2, 16, 128, 4, 0, 0.1, 0,
+                            None) == -1  # null Q
+    # decode: GQA group of 3 unsupported, bad split count, missing workspace
+    assert L.swa_decode_ex(FAKE, FAKE, FAKE, FAKE, 1, 6, 2, 128, 8, 0, 0.1, FAKE, None, 0, 0,
+                           None, 0, None) == -2
+    assert L.swa_decode_ex(FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 128, 8, 0, 0.1, FAKE, None, 0, 2000,
+                           None, 0, None) == -1
+    assert L.swa_decode_ex(FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 128, 8, 0, 0.1, FAKE, None, 0, 4,
+                           None, 0, None) == -6
+    assert L.swa_decode_workspace_bytes(2, 4, 2, 128, 8, 0, 4) == 2 * 4 * 4 * 130 * 4
+    assert L.swa_decode_workspace_bytes(2, 4, 2, 128, 8, 0, 1) == 0
+    # append: negative T, misaligned cache; T == 0 is a no-op
+    assert L.swa_cache_append(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 1, 2, 128, 8, 0, 0, None) == -1
+    assert L.swa_cache_append(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 1, 1, 2, 128, 8, 0, 0, None) == -1
+    assert L.swa_cache_append(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 2, 128, 8, 0, 0, None) == 0
