@@ -37,7 +37,12 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-PREFILL = dict(B=1, H=32, Hkv=8, n=16384, d=128, w=4096, g=0)
+PREFILL_WORKLOADS = {
+    "mistral_like_prefill": dict(B=1, H=32, Hkv=8, n=16384, d=128, w=4096, g=0, sink_scale=1.0),
+    "gemma3_local_prefill": dict(B=2, H=32, Hkv=16, n=32768, d=128, w=1024, g=0, sink_scale=1.0),
+    "long_sink_prefill": dict(B=1, H=32, Hkv=8, n=131072, d=128, w=4096, g=4, sink_scale=4.0),
+}
+PREFILL = PREFILL_WORKLOADS["mistral_like_prefill"]
 DECODE = dict(B=32, H=32, Hkv=8, d=128, w=4096, g=4, pos=100000, sink_scale=4.0)
 METRIC = "SWA prefill useful TFLOP/s (% bf16 peak); decode HBM GB/s (% peak)"
 PREFILL_KERNEL_SRC = os.path.join(ROOT, "sink_sparse_attention_swa_b300", "csrc", "swa_prefill_tc.cu")
@@ -179,20 +184,27 @@ def barrier(world):
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def cpu_oracle_sample(min_seconds=10.0, max_seconds=30.0, seed=0):
-    """Times the fp64 oracle on sampled query rows of the prefill workload until
+_CPU_INPUTS = {}
+
+
+def cpu_oracle_sample(min_seconds=10.0, max_seconds=30.0, seed=0, c=None):
+    """Times the fp64 oracle on sampled query rows of a prefill workload until
     at least `min_seconds` have passed.  Returns (TFLOP/s of useful work,
     rows, seconds, threads)."""
     import oracle
     from sink_sparse_attention_swa_b300 import synthetic
 
     oracle.set_num_threads(os.cpu_count() or 1)
-    c = PREFILL
-    x = synthetic.prefill_inputs(c["B"], c["H"], c["Hkv"], c["n"], c["d"], c["w"], c["g"],
-                                 dtype="bf16", seed=seed, device="cpu")
-    K = x.K.double().numpy()
-    V = x.V.double().numpy()
-    rows_all = synthetic.sample_rows(c["B"], c["H"], c["n"], 1 << 14, seed=1).numpy()
+    c = PREFILL if c is None else c
+    key = (tuple(sorted(c.items())), seed)
+    if key not in _CPU_INPUTS:
+        x = synthetic.prefill_inputs(c["B"], c["H"], c["Hkv"], c["n"], c["d"], c["w"], c["g"],
+                                     dtype="bf16", seed=seed, sink_scale=c["sink_scale"],
+                                     device="cpu")
+        _CPU_INPUTS[key] = (x, x.K.double().numpy(), x.V.double().numpy())
+    x, K, V = _CPU_INPUTS[key]
+    rows_all = synthetic.sample_rows(c["B"], c["H"], c["n"], min(1 << 20, c["B"] * c["H"] * c["n"]),
+                                     seed=1).numpy()
     done, t_total, flops = 0, 0.0, 0
     batch = 64
     while t_total < min_seconds and done < rows_all.shape[0]:
@@ -237,45 +249,101 @@ def run_swa(args):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     pk = peaks()
-    c = PREFILL
-    x = synthetic.prefill_inputs(c["B"], c["H"], c["Hkv"], c["n"], c["d"], c["w"], c["g"],
-                                 dtype="bf16", seed=rank, device=dev)
-    out = torch.empty_like(x.Q)
+    c = PREFILL_WORKLOADS[args.workload]
     flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MiB > L2
-    fn = lambda: swa.prefill(x.Q, x.K, x.V, c["w"], c["g"], x.scale, out=out, stream=stream)
-
-    barrier(world)
-    torch.cuda.synchronize()
-    with Clocks(local) as clk:
-        times = time_launches(fn, args.steps, args.warmup, flush, stream)
-    barrier(world)
-    ms = max_over_ranks(float(np.mean(times)), world, dev)
     flops = prefill_flops(c)
-    value = flops * world / (ms * 1e-3) / 1e12
-    launch_ms = float(np.mean(times))
-    achieved = flops / (launch_ms * 1e-3) / 1e12
-    traffic = recorded_traffic("swa_prefill_bf16_sm103", "mistral_like_prefill", PREFILL_KERNEL_SRC)
+    ms = value = achieved = traffic = None
+    clk_summary = None
+    e2e = None
+    if args.only in ("all", "prefill"):
+        x = synthetic.prefill_inputs(c["B"], c["H"], c["Hkv"], c["n"], c["d"], c["w"], c["g"],
+                                     dtype="bf16", seed=rank, sink_scale=c["sink_scale"],
+                                     device=dev)
+        out = torch.empty_like(x.Q)
+        fn = lambda: swa.prefill(x.Q, x.K, x.V, c["w"], c["g"], x.scale, out=out, stream=stream)
+        barrier(world)
+        torch.cuda.synchronize()
+        with Clocks(local) as clk:
+            times = time_launches(fn, args.steps, args.warmup, flush, stream)
+        barrier(world)
+        clk_summary = clk.summary()
+        ms = max_over_ranks(float(np.mean(times)), world, dev)
+        value = flops * world / (ms * 1e-3) / 1e12
+        launch_ms = float(np.mean(times))
+        achieved = flops / (launch_ms * 1e-3) / 1e12
+        traffic = recorded_traffic("swa_prefill_bf16_sm103", args.workload, PREFILL_KERNEL_SRC)
 
-    # ---- end to end through the public API with host buffers
-    Qh = x.Q.cpu().pin_memory()
-    Kh = x.K.cpu().pin_memory()
-    Vh = x.V.cpu().pin_memory()
-    Oh = torch.empty_like(Qh).pin_memory()
-    Qd, Kd, Vd = torch.empty_like(x.Q), torch.empty_like(x.K), torch.empty_like(x.V)
+        if not args.no_e2e:
+            # ---- end to end through the public API with host buffers
+            Qh = x.Q.cpu().pin_memory()
+            Kh = x.K.cpu().pin_memory()
+            Vh = x.V.cpu().pin_memory()
+            Oh = torch.empty_like(Qh).pin_memory()
+            Qd, Kd, Vd = torch.empty_like(x.Q), torch.empty_like(x.K), torch.empty_like(x.V)
 
-    def e2e_step():
-        Qd.copy_(Qh, non_blocking=True)
-        Kd.copy_(Kh, non_blocking=True)
-        Vd.copy_(Vh, non_blocking=True)
-        swa.prefill(Qd, Kd, Vd, c["w"], c["g"], x.scale, out=out, stream=stream)
-        Oh.copy_(out, non_blocking=True)
+            def e2e_step():
+                Qd.copy_(Qh, non_blocking=True)
+                Kd.copy_(Kh, non_blocking=True)
+                Vd.copy_(Vh, non_blocking=True)
+                swa.prefill(Qd, Kd, Vd, c["w"], c["g"], x.scale, out=out, stream=stream)
+                Oh.copy_(out, non_blocking=True)
 
-    e2e_times = time_launches(e2e_step, max(2, args.steps // 2), 2, flush, stream)
-    e2e_ms = max_over_ranks(float(np.mean(e2e_times)), world, dev)
-    h2d = (Qh.numel() + Kh.numel() + Vh.numel()) * 2
-    d2h = Oh.numel() * 2
+            e2e_times = time_launches(e2e_step, max(2, args.steps // 2), 2, flush, stream)
+            e2e_ms = max_over_ranks(float(np.mean(e2e_times)), world, dev)
+            e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": (Qh.numel() + Kh.numel() + Vh.numel()) * 2,
+                   "d2h_bytes_per_step": Oh.numel() * 2, "ms_per_step": e2e_ms}
+            del Qh, Kh, Vh, Oh, Qd, Kd, Vd
+        del x, out
+        torch.cuda.empty_cache()
 
     # ---- decode leg: append one token + decode, streaming-decode workload
+    decode_line = None
+    if args.only in ("all", "decode"):
+        decode_line = decode_leg(args, swa, synthetic, world, rank, local, dev, stream, flush, pk)
+
+    cpu = None
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline
+            and args.only in ("all", "prefill")):
+        tfl, rows, secs, thr = cpu_oracle_sample(args.cpu_seconds, 3 * args.cpu_seconds, c=c)
+        cpu = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"{rows} query rows of {args.workload} (uniformly sampled over "
+                         f"heads and positions), fp64, {secs:.1f} s"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, **c, "scale": "1/sqrt(d)",
+                   "l2": "flushed before each timed launch (256 MiB write)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "clocks": clk_summary,
+        "e2e": e2e,
+        "gpu_launches": args.steps if value is not None else 0,
+        "roofline": None if value is None else {
+            "bound": "tensor", "achieved": achieved, "peak": pk["bf16"],
+            "unit": "TFLOP/s", "frac": achieved / pk["bf16"], "traffic": traffic,
+            "kernel": "swa_prefill_bf16_sm103", "peak_source": pk["src"] + " burst",
+            "frac_of_sustained": achieved / pk["bf16_sustained"],
+            "useful_flops_per_launch": flops},
+        "cpu_baseline": cpu,
+        "decode": decode_line,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def decode_leg(args, swa, synthetic, world, rank, local, dev, stream, flush, pk):
     dc = DECODE
     dx = synthetic.decode_cache_inputs(dc["B"], dc["H"], dc["Hkv"], dc["d"], dc["w"], dc["g"],
                                        dc["pos"], dtype="bf16", seed=rank,
@@ -302,55 +370,16 @@ def run_swa(args):
     dec_ms = float(np.mean(dec_only))
     dec_traffic = recorded_traffic("swa_decode_split", "streaming_decode_sinks", DECODE_KERNEL_SRC)
     assert swa.device_status(stream) == 0, "device status reported an error"
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tfl, rows, secs, thr = cpu_oracle_sample(args.cpu_seconds, 3 * args.cpu_seconds)
-        cpu = {"value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-               "sample": f"{rows} query rows of the Mistral-like prefill (uniformly sampled over "
-                         f"heads and positions), fp64, {secs:.1f} s"}
-
-    if rank != 0:
-        return
-    line = {
-        "metric": METRIC,
-        "value": value,
-        "unit": "TFLOP/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": ms,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": "mistral_like_prefill", **c, "scale": "1/sqrt(d)",
-                   "l2": "flushed before each timed launch (256 MiB write)",
-                   "parallelism": f"replicas{world}" if world > 1 else "single"},
-        "clocks": clk.summary(),
-        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"],
-                     "unit": "TFLOP/s", "frac": achieved / pk["bf16"], "traffic": traffic,
-                     "kernel": "swa_prefill_bf16_sm103", "peak_source": pk["src"] + " burst",
-                     "frac_of_sustained": achieved / pk["bf16_sustained"],
-                     "useful_flops_per_launch": flops},
-        "cpu_baseline": cpu,
-        "decode": {"workload": "streaming_decode_sinks", **{k: dc[k] for k in dc},
-                   "value": dgbs, "unit": "GB/s", "ms_per_step": dms,
-                   "step": "cache append (1 token) + decode",
-                   "roofline": {"bound": "hbm", "achieved": dbytes / (dec_ms * 1e-3) / 1e9,
-                                "peak": pk["hbm"], "unit": "GB/s",
-                                "frac": dbytes / (dec_ms * 1e-3) / 1e9 / pk["hbm"],
-                                "traffic": dec_traffic, "kernel": "swa_decode_split + merge",
-                                "decode_only_ms": dec_ms, "algorithmic_bytes": dbytes,
-                                "frac_of_8TBs": dbytes / (dec_ms * 1e-3) / 1e9 / 8000.0},
-                   "clocks": dclk.summary(), "gpu_launches": dsteps * 3},
-    }
-    print(json.dumps(line), flush=True)
+    return {"workload": "streaming_decode_sinks", **{k: dc[k] for k in dc},
+            "value": dgbs, "unit": "GB/s", "ms_per_step": dms,
+            "step": "cache append (1 token) + decode",
+            "roofline": {"bound": "hbm", "achieved": dbytes / (dec_ms * 1e-3) / 1e9,
+                         "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": dbytes / (dec_ms * 1e-3) / 1e9 / pk["hbm"],
+                         "traffic": dec_traffic, "kernel": "swa_decode_split + merge",
+                         "decode_only_ms": dec_ms, "algorithmic_bytes": dbytes,
+                         "frac_of_8TBs": dbytes / (dec_ms * 1e-3) / 1e9 / 8000.0},
+            "clocks": dclk.summary(), "gpu_launches": dsteps * 3}
 
 
 def run_reference(args):
@@ -383,7 +412,8 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "mistral_like_prefill", **PREFILL, "scale": "1/sqrt(d)"},
+        "config": {"workload": "mistral_like_prefill", **PREFILL, "scale": "1/sqrt(d)",
+                   "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                          "sample": f"{rows_total} sampled query rows over {args.steps} steps, "
                                    f"{secs:.1f} s of fp64 CPU work; ms_per_step extrapolates "
@@ -403,6 +433,9 @@ def main():
     ap.add_argument("--impl", default="swa", choices=["swa", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"])
+    ap.add_argument("--workload", default="mistral_like_prefill", choices=sorted(PREFILL_WORKLOADS))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
