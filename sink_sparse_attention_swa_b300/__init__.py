@@ -4,8 +4,8 @@ A thin ctypes binding over ``libswa.so`` (C ABI in ``include/swa.h``).  The
 functions here only marshal arguments -- shapes, dtypes, pointers, the stream
 -- and call the library; every step of the computation runs in the library's
 CUDA kernels.  Tensors are torch CUDA tensors (torch is used for device memory
-and streams only).  If the library is missing the import fails: there is no
-fallback.
+and streams only).  The library is loaded on first use; if it is missing that
+first call raises ImportError: there is no fallback.
 
     prefill(q, k, v, w, g=0, scale=None, out=None, lse=None)        -> out
     decode(q, k_cache, v_cache, pos, w, g=0, scale=None, ...)        -> out
@@ -58,7 +58,13 @@ class SwaError(RuntimeError):
         self.status = status
 
 
+_LIB = None
+
+
 def _load():
+    global _LIB
+    if _LIB is not None:
+        return _LIB
     if not os.path.exists(_LIB_PATH):
         raise ImportError(
             f"libswa.so not found at {_LIB_PATH}; build it with "
@@ -68,10 +74,14 @@ def _load():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
+    _LIB = lib
     return lib
 
 
-lib = _load()
+def __getattr__(name):
+    if name == "lib":
+        return _load()
+    raise AttributeError(name)
 
 
 def library_path() -> str:
@@ -121,14 +131,14 @@ def prefill(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None, l
     if lse is not None:
         _need(lse, "lse", torch.float32, (B, H, n))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    rc = lib.swa_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, n, d,
+    rc = _load().swa_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, n, d,
                             int(w), int(g), scale, _DT[q.dtype], _stream(stream, q.device))
     _check("swa_prefill_ex", rc)
     return out
 
 
 def decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits=0) -> int:
-    return int(lib.swa_decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits))
+    return int(_load().swa_decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits))
 
 
 def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = None, out=None,
@@ -148,7 +158,7 @@ def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = N
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     st = _stream(stream, q.device)
     if workspace is None and lse is None and num_splits == 0 and q.dtype == torch.bfloat16:
-        rc = lib.swa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Hkv, d,
+        rc = _load().swa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Hkv, d,
                             int(w), int(g), scale, _ptr(out), st)
         _check("swa_decode", rc)
         return out
@@ -158,7 +168,7 @@ def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = N
     if workspace is None and nbytes > 0:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.swa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Hkv, d,
+    rc = _load().swa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Hkv, d,
                            int(w), int(g), scale, _ptr(out), _ptr(lse), _DT[q.dtype],
                            int(num_splits), _ptr(workspace), ws_bytes, st)
     _check("swa_decode_ex", rc)
@@ -177,33 +187,33 @@ def cache_append(k_cache, v_cache, k_new, v_new, pos0, w: int, g: int = 0, strea
     _need(k_new, "k_new", k_cache.dtype, (B, Hkv, T, d))
     _need(v_new, "v_new", k_cache.dtype, (B, Hkv, T, d))
     _need(pos0, "pos0", torch.int32, (B,))
-    rc = lib.swa_cache_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos0),
+    rc = _load().swa_cache_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos0),
                               T, B, Hkv, d, int(w), int(g), _DT[k_cache.dtype],
                               _stream(stream, k_cache.device))
     _check("swa_cache_append", rc)
 
 
 def count_pairs(n: int, w: int, g: int) -> int:
-    return int(lib.swa_count_pairs(n, w, g))
+    return int(_load().swa_count_pairs(n, w, g))
 
 
 def enumerate_tiles(n: int, w: int, g: int, BM: int, BN: int):
     """Tile classes [ceil(n/BM), ceil(n/BN)] as a torch int32 CPU tensor."""
     nq, nk = -(-n // BM), -(-n // BN)
     out = torch.zeros(nq, nk, dtype=torch.int32)
-    _check("swa_enumerate_tiles", lib.swa_enumerate_tiles(n, w, g, BM, BN, out.data_ptr(), out.numel()))
+    _check("swa_enumerate_tiles", _load().swa_enumerate_tiles(n, w, g, BM, BN, out.data_ptr(), out.numel()))
     return out
 
 
 def cache_slot(p: int, w: int, g: int):
     r, s = ctypes.c_int32(), ctypes.c_int32()
-    _check("swa_cache_slot", lib.swa_cache_slot(p, w, g, ctypes.byref(r), ctypes.byref(s)))
+    _check("swa_cache_slot", _load().swa_cache_slot(p, w, g, ctypes.byref(r), ctypes.byref(s)))
     return r.value, s.value
 
 
 def device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status code."""
-    return int(lib.swa_get_device_status(_stream(stream, None)))
+    return int(_load().swa_get_device_status(_stream(stream, None)))
 
 
 def selftest_umma(A, Bk, Bn, stream=None):
@@ -213,6 +223,6 @@ def selftest_umma(A, Bk, Bn, stream=None):
         _need(t, nm, torch.bfloat16, (128, 128))
     D1 = torch.empty(128, 128, dtype=torch.float32, device=A.device)
     D2 = torch.empty_like(D1)
-    _check("swa_selftest_umma", lib.swa_selftest_umma(_ptr(A), _ptr(Bk), _ptr(Bn), _ptr(D1),
+    _check("swa_selftest_umma", _load().swa_selftest_umma(_ptr(A), _ptr(Bk), _ptr(Bn), _ptr(D1),
                                                       _ptr(D2), _stream(stream, A.device)))
     return D1, D2
