@@ -140,6 +140,29 @@ int swa_cache_append(void *Kcache, void *Vcache, const void *k_new, const void *
                      const int32_t *pos0, int T, int B, int Hkv, int d, int w, int g,
                      swa_dtype dtype, swa_stream_t stream);
 
+/*
+ * swa_decode_noalloc -- swa_decode for callers that cannot allocate device
+ * memory: plugins and embedded runtimes handed only their input and output
+ * buffers, processes whose device memory belongs to another allocator, and
+ * latency-critical loops where cudaMalloc/cudaFree (and the synchronisation
+ * a free implies) are not allowed.  The pages have no counterpart: this is an
+ * interface variant, not part of the method.
+ * Same arguments, semantics and result as swa_decode (bf16).  It allocates
+ * nothing: the split-K partial results go to a fixed array of
+ * SWA_NOALLOC_SCRATCH_BYTES in the library's own device memory, present on
+ * every GPU that loads the library until the process exits.  Sizes whose
+ * workspace (swa_decode_workspace_bytes(..., 0)) exceeds that array return
+ * SWA_ERR_WORKSPACE and enqueue nothing.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  All calls share the array
+ * and it keeps the last call's contents (nothing needs to start at zero);
+ * calls whose kernels overlap on the GPU race and must be serialised.
+ */
+#define SWA_NOALLOC_SCRATCH_BYTES (4u << 20)
+int swa_decode_noalloc(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos,
+                       int B, int H, int Hkv, int d, int w, int g, float scale, void *O,
+                       swa_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Host helpers (no GPU needed).                                           */
 /* ---------------------------------------------------------------------- */

@@ -41,6 +41,7 @@ SIGNATURES = {
     "swa_decode": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p]),
     "swa_decode_workspace_bytes": (_sz, [_i] * 7),
     "swa_decode_ex": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p, _i, _i, _p, _sz, _p]),
+    "swa_decode_noalloc": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p]),
     "swa_cache_append": (_i, [_p, _p, _p, _p, _p] + [_i] * 6 + [_i, _p]),
     "swa_count_pairs": (_i64, [_i64, _i64, _i64]),
     "swa_enumerate_tiles": (_i, [_i64, _i64, _i64, _i, _i, _p, _sz]),

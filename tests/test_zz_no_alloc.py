@@ -1,0 +1,60 @@
+"""swa_decode_noalloc: the decode entry point for callers that cannot allocate
+device memory (plugins handed only their buffers, processes whose memory
+belongs to another allocator, loops where cudaMalloc/cudaFree are not
+allowed).  It keeps its split partials in a fixed array inside the library.
+
+Called through the C ABI and compared with swa_decode (the entry point that
+allocates its workspace) on two calls in a row, since the array is shared and
+keeps the previous call's contents.  This file is collected last on purpose.
+"""
+import pytest
+import torch
+
+from sink_sparse_attention_swa_b300 import synthetic
+from tests.parity import assert_close
+
+SWA_ERR_WORKSPACE = -6
+
+
+def call_noalloc(swa, x, out, w, g):
+    B, H, d = x.q.shape
+    Hkv = x.Kc.shape[1]
+    return swa.lib.swa_decode_noalloc(
+        x.q.data_ptr(), x.Kc.data_ptr(), x.Vc.data_ptr(), x.pos.data_ptr(), B, H, Hkv, d, w, g,
+        x.scale, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.gpu
+def test_noalloc_decode_matches_swa_decode_twice(swa):
+    cases = [
+        # the streaming-decode workload: B=32 H=32 Hkv=8 d=128 w=4096 g=4, pos=100000
+        dict(B=32, H=32, Hkv=8, d=128, w=4096, g=4, pos=100000, seed=0),
+        # a different shape second, so the shared array holds another call's data
+        dict(B=3, H=8, Hkv=2, d=128, w=300, g=2, pos=[5, 299, 1000], seed=1),
+    ]
+    for c in cases:
+        x = synthetic.decode_cache_inputs(c["B"], c["H"], c["Hkv"], c["d"], c["w"], c["g"],
+                                          c["pos"], dtype="bf16", seed=c["seed"], sink_scale=4.0,
+                                          device="cuda")
+        ref = swa.decode(x.q, x.Kc, x.Vc, x.pos, c["w"], c["g"], x.scale)  # swa_decode
+        torch.cuda.synchronize()
+        for _ in range(2):
+            out = torch.full_like(x.q, float("nan"))
+            assert call_noalloc(swa, x, out, c["w"], c["g"]) == 0
+            torch.cuda.synchronize()
+            assert_close(out, ref.double().cpu().numpy(), "bf16", f"noalloc {c}")
+    assert swa.device_status() == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_sizes_beyond_the_array(swa):
+    # 64 sequences x 64 heads x 3 splits x (128+2) fp32 = 6.4 MB > 4 MiB
+    B, H, Hkv, d, w, g = 64, 64, 8, 128, 65536, 0
+    need = swa.decode_workspace_bytes(B, H, Hkv, d, w, g)
+    assert need > (4 << 20)
+    dummy = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    pos = torch.zeros(B, dtype=torch.int32, device="cuda")
+    rc = swa.lib.swa_decode_noalloc(dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(),
+                                    pos.data_ptr(), B, H, Hkv, d, w, g, 0.1, dummy.data_ptr(),
+                                    torch.cuda.current_stream().cuda_stream)
+    assert rc == SWA_ERR_WORKSPACE
