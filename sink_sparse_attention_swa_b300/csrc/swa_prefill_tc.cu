@@ -32,6 +32,7 @@
 //    drained with bounded waits, and TMEM is freed before exit.
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "swa_internal.h"
@@ -480,6 +481,437 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ------------------------------------------------------------------------
+// Pair kernel: two query heads of one GQA group per work item.
+//
+// The two heads read the same key/value tiles, so each K/V tile staged in
+// shared memory feeds four MMAs (S_A, S_B, P_A V, P_B V) instead of two.  Two
+// softmax warpgroups (A: warps 2-5, B: warps 6-9) work on the two heads and
+// take turns with the tensor core; the MMA warp issues, per key tile c,
+//     P_A(c-1) V, S_A(c) = Q_A K^T, P_B(c-1) V, S_B(c) = Q_B K^T
+// so softmax A(c) runs while the tensor core computes P_B(c-1) V and S_B(c),
+// and the other way round.  TMEM (512 columns): O_A [0,128), S_A [128,256),
+// O_B [256,384), S_B [384,512); P (bf16) is written back over the first half
+// of its S buffer.  A tcgen05.commit tracks every MMA issued before it, so the
+// S_X(c) barrier also tells softmax X that P_X(c-1) V has landed in O_X and
+// that O_X may be rescaled.
+// ------------------------------------------------------------------------
+constexpr int NTHREADS2 = 320;
+
+template <int HD>
+struct Layout2 {
+    static constexpr uint32_t QB = BM * HD * 2;
+    static constexpr uint32_t KB = BN * HD * 2;
+    static constexpr uint32_t Q_OFF = 0;  // Q_A, Q_B
+    static constexpr uint32_t K_OFF = Q_OFF + 2 * QB;
+    static constexpr uint32_t V_OFF = K_OFF + STAGES * KB;
+    static constexpr uint32_t BAR_OFF = V_OFF + STAGES * KB;
+    enum {
+        Q_FULL = 0,
+        Q_EMPTY = 2,
+        K_FULL = 4,
+        V_FULL = K_FULL + STAGES,
+        KV_EMPTY = V_FULL + STAGES,
+        S_FULL = KV_EMPTY + STAGES,
+        P_FULL = S_FULL + 2,
+        O_FULL = P_FULL + 2,
+        O_EMPTY = O_FULL + 2,
+        DRAIN = O_EMPTY + 2,
+        NBAR = DRAIN + 1
+    };
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t BYTES = MISC_OFF + 16;
+    static constexpr uint32_t DYN_SMEM = (BYTES + 1024 > 120 * 1024) ? BYTES + 1024 : 120 * 1024;
+};
+
+__device__ __forceinline__ void decode_pair_item(int t, const PrefillParams &p, int &b, int &h0,
+                                                 int &kvh, int &qt)
+{
+    const int pairs = p.G >> 1;
+    const int hp = t % pairs;
+    t /= pairs;
+    qt = t % p.n_qt;
+    t /= p.n_qt;
+    kvh = t % p.Hkv;
+    b = t / p.Hkv;
+    h0 = kvh * p.G + 2 * hp;
+}
+
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Softmax over 64 columns (two 32-column halves of s) of one row: p =
+// exp2(s * sl2 - m), accumulated into the pair-sum `acc2`, packed to bf16 pairs.
+__device__ __forceinline__ void softmax_half(const uint32_t (&sa)[32], const uint32_t (&sb)[32],
+                                             uint64_t sl2x2, uint64_t negm2, uint64_t &acc2,
+                                             uint32_t (&pk)[32])
+{
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        float x0, x1, y0, y1;
+        unpack2(fma2(pack2(sa[e], sa[e + 1]), sl2x2, negm2), x0, x1);
+        unpack2(fma2(pack2(sb[e], sb[e + 1]), sl2x2, negm2), y0, y1);
+        const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(y0), p3 = ex2(y1);
+        acc2 = add2(acc2, add2(pack2(__float_as_uint(p0), __float_as_uint(p1)),
+                               pack2(__float_as_uint(p2), __float_as_uint(p3))));
+        pk[e >> 1] = pack_bf16x2(p0, p1);
+        pk[16 + (e >> 1)] = pack_bf16x2(p2, p3);
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(NTHREADS2, 1)
+    swa_prefill_bf16_pair_sm103(const __grid_constant__ CUtensorMap tmQ,
+                                const __grid_constant__ CUtensorMap tmK,
+                                const __grid_constant__ CUtensorMap tmV, const PrefillParams p)
+{
+    using L = Layout2<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t sQ = sb + L::Q_OFF, sK = sb + L::K_OFF, sV = sb + L::V_OFF;
+    const uint32_t bars = sb + L::BAR_OFF;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pairs_per_item_count = p.num_items;
+#define BAR(i) (bars + 8u * static_cast<uint32_t>(i))
+
+    if (threadIdx.x == 0) {
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(BAR(L::Q_FULL + x), 1);
+            mbar_init(BAR(L::Q_EMPTY + x), 1);
+            mbar_init(BAR(L::S_FULL + x), 1);
+            mbar_init(BAR(L::P_FULL + x), 4);
+            mbar_init(BAR(L::O_FULL + x), 1);
+            mbar_init(BAR(L::O_EMPTY + x), 4);
+        }
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(BAR(L::K_FULL + i), 1);
+            mbar_init(BAR(L::V_FULL + i), 1);
+            mbar_init(BAR(L::KV_EMPTY + i), 1);
+        }
+        mbar_init(BAR(L::DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch(&tmQ);
+        tma_prefetch(&tmK);
+        tma_prefetch(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int kv_iter = 0, it = 0;
+            int last_k_par[STAGES], last_q_par[2] = {-1, -1};
+            for (int s = 0; s < STAGES; ++s) last_k_par[s] = -1;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < pairs_per_item_count; t += gridDim.x, ++it) {
+                int b, h0, kvh, qt;
+                decode_pair_item(t, p, b, h0, kvh, qt);
+                const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+                for (int x = 0; x < 2 && ok; ++x) {
+                    if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
+                                   TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(BAR(L::Q_FULL + x), L::QB);
+                    for (int c = 0; c < HD / 64; ++c)
+                        tma_load_3d(sQ + x * L::QB + c * (BM * 128), &tmQ, BAR(L::Q_FULL + x),
+                                    c * 64, qt * BM, b * p.H + h0 + x);
+                    last_q_par[x] = it & 1;
+                }
+                for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
+                    const int st = kv_iter % STAGES;
+                    const uint32_t ph = (kv_iter / STAGES) & 1;
+                    if (!mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status,
+                                   TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    const int k0 = tile_kt(tr, j) * BN;
+                    const int zkv = b * p.Hkv + kvh;
+                    mbar_expect_tx(BAR(L::K_FULL + st), L::KB);
+                    for (int c = 0; c < HD / 64; ++c)
+                        tma_load_3d(sK + st * L::KB + c * (BN * 128), &tmK, BAR(L::K_FULL + st),
+                                    c * 64, k0, zkv);
+                    mbar_expect_tx(BAR(L::V_FULL + st), L::KB);
+                    for (int c = 0; c < HD / 64; ++c)
+                        tma_load_3d(sV + st * L::KB + c * (BN * 128), &tmV, BAR(L::V_FULL + st),
+                                    c * 64, k0, zkv);
+                    last_k_par[st] = static_cast<int>(ph);
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < STAGES; ++s)
+                    if (last_k_par[s] >= 0) {
+                        mbar_wait(BAR(L::K_FULL + s), last_k_par[s], nullptr, nullptr, TIMEOUT_NS);
+                        mbar_wait(BAR(L::V_FULL + s), last_k_par[s], nullptr, nullptr, TIMEOUT_NS);
+                    }
+                for (int x = 0; x < 2; ++x)
+                    if (last_q_par[x] >= 0)
+                        mbar_wait(BAR(L::Q_FULL + x), last_q_par[x], nullptr, nullptr, TIMEOUT_NS);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(128, BN, 0);
+            const uint32_t idesc_o = idesc_bf16_f32(128, HD, 1);
+            int kv_iter = 0, it = 0, c = 0;
+            bool ok = true;
+            bool have_prev = false, prev_first = false, prev_last = false;
+            int prev_st = 0, prev_c = 0, prev_it = 0;
+            uint32_t prev_ph = 0;
+            // P_X(prev) V into O_X
+            auto issue_pv = [&](int x) -> bool {
+                if (!mbar_wait(BAR(L::P_FULL + x), prev_c & 1, abort_flag, p.status, TIMEOUT_NS))
+                    return false;
+                if (x == 0 &&
+                    !mbar_wait(BAR(L::V_FULL + prev_st), prev_ph, abort_flag, p.status, TIMEOUT_NS))
+                    return false;
+                if (prev_first && !mbar_wait(BAR(L::O_EMPTY + x), (prev_it & 1) ^ 1, abort_flag,
+                                             p.status, TIMEOUT_NS))
+                    return false;
+                tc_fence_after();
+                const uint32_t vbase = sV + prev_st * L::KB;
+                const uint32_t o_col = x * 256, p_col = x * 256 + 128;
+                for (int ks = 0; ks < BN / 16; ++ks) {
+                    const uint64_t bdesc = smem_desc_sw128(vbase + ks * (16 * 128), BN * 128, 1024);
+                    mma_ts(tmem + o_col, tmem + p_col + ks * 8, bdesc, idesc_o,
+                           (!prev_first || ks > 0) ? 1u : 0u);
+                }
+                if (x == 1) tc_commit(BAR(L::KV_EMPTY + prev_st));
+                if (prev_last) tc_commit(BAR(L::O_FULL + x));
+                return true;
+            };
+            auto issue_s = [&](int x, int st, bool last) {
+                const uint32_t qbase = sQ + x * L::QB, kbase = sK + st * L::KB;
+                for (int ks = 0; ks < HD / 16; ++ks) {
+                    const uint32_t blk = ks >> 2, sub = ks & 3;
+                    const uint64_t adesc =
+                        smem_desc_sw128(qbase + blk * (BM * 128) + sub * 32, 16, 1024);
+                    const uint64_t bdesc =
+                        smem_desc_sw128(kbase + blk * (BN * 128) + sub * 32, 16, 1024);
+                    mma_ss(tmem + x * 256 + 128, adesc, bdesc, idesc_s, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(BAR(L::S_FULL + x));
+                if (last) tc_commit(BAR(L::Q_EMPTY + x));
+            };
+            for (int t = blockIdx.x; ok && t < pairs_per_item_count; t += gridDim.x, ++it) {
+                int b, h0, kvh, qt;
+                decode_pair_item(t, p, b, h0, kvh, qt);
+                const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+                for (int j = 0; j < tr.count; ++j, ++kv_iter, ++c) {
+                    const int st = kv_iter % STAGES;
+                    const uint32_t ph = (kv_iter / STAGES) & 1;
+                    const bool last = (j == tr.count - 1);
+                    for (int x = 0; x < 2; ++x) {
+                        if (have_prev && !issue_pv(x)) {
+                            ok = false;
+                            break;
+                        }
+                        if (j == 0 && !mbar_wait(BAR(L::Q_FULL + x), it & 1, abort_flag, p.status,
+                                                 TIMEOUT_NS)) {
+                            ok = false;
+                            break;
+                        }
+                        if (x == 0 && !mbar_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status,
+                                                 TIMEOUT_NS)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_s(x, st, last);
+                    }
+                    if (!ok) break;
+                    have_prev = true;
+                    prev_st = st;
+                    prev_ph = ph;
+                    prev_c = c;
+                    prev_it = it;
+                    prev_first = (j == 0);
+                    prev_last = last;
+                }
+            }
+            if (ok && have_prev) {
+                if (issue_pv(0)) issue_pv(1);
+            }
+            tc_commit(BAR(L::DRAIN));
+            mbar_wait(BAR(L::DRAIN), 0, nullptr, nullptr, TIMEOUT_NS);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax A / B
+        const int x = (warp - 2) >> 2;           // 0: head h0 (warps 2-5), 1: h0+1 (warps 6-9)
+        const int sub = warp & 3;                // TMEM lane quarter this warp may access
+        const int r = sub * 32 + lane;           // query row within the tile
+        const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
+        const uint32_t o_addr = tmem + lane_off + x * 256;
+        const uint32_t s_addr = o_addr + 128;
+        const float sl2 = p.sl2;
+        const uint64_t sl2x2 = pack2(__float_as_uint(sl2), __float_as_uint(sl2));
+        int c = 0, it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < pairs_per_item_count; t += gridDim.x, ++it) {
+            int b, h0, kvh, qt;
+            decode_pair_item(t, p, b, h0, kvh, qt);
+            const int h = h0 + x;
+            const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+            const int i = tr.q0 + r;
+            const int lo = i - p.w + 1;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < tr.count; ++j, ++c) {
+                if (!warp_wait(BAR(L::S_FULL + x), c & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t s[4][32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_ld32(s_addr + q * 32, s[q]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) reg_fence32(s[q]);
+                const int kt = tile_kt(tr, j);
+                const int k0 = kt * BN;
+                if (!tile_full(tr, kt, p.w, p.g, BN)) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int jj = k0 + q * 32 + e;
+                            const bool allowed = (jj <= i) && (jj >= lo || jj < p.g);
+                            if (!allowed) s[q][e] = __float_as_uint(-INFINITY);
+                        }
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    mx0 = max3(mx0, __uint_as_float(s[0][e]), __uint_as_float(s[0][e + 1]));
+                    mx1 = max3(mx1, __uint_as_float(s[1][e]), __uint_as_float(s[1][e + 1]));
+                    mx2 = max3(mx2, __uint_as_float(s[2][e]), __uint_as_float(s[2][e + 1]));
+                    mx3 = max3(mx3, __uint_as_float(s[3][e]), __uint_as_float(s[3][e + 1]));
+                }
+                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const float m_new = fmaxf(m, m_tile);
+                if (j == 0) {
+                    m = m_new;
+                } else {
+                    const bool need = m_new > m + RESCALE_LOG2;
+                    if (__any_sync(0xffffffffu, need)) {
+                        // O_X is complete: the S_X(c) commit covered P_X(c-1) V
+                        const float alpha = need ? ex2(m - m_new) : 1.f;
+                        if (need) m = m_new;
+                        l *= alpha;
+#pragma unroll 1
+                        for (int q = 0; q < HD / 32; ++q) {
+                            uint32_t o[32];
+                            tmem_ld32(o_addr + q * 32, o);
+                            tmem_ld_wait();
+                            reg_fence32(o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(o_addr + q * 32, o);
+                        }
+                    }
+                }
+                const float m_use = (m == -INFINITY) ? 0.f : m;
+                const uint64_t negm2 = pack2(__float_as_uint(-m_use), __float_as_uint(-m_use));
+                uint64_t acc2 = 0;  // two fp32 zeros
+                uint32_t pk[32];
+                softmax_half(s[0], s[1], sl2x2, negm2, acc2, pk);
+                tmem_st32(s_addr, pk);
+                softmax_half(s[2], s[3], sl2x2, negm2, acc2, pk);
+                tmem_st32(s_addr + 32, pk);
+                float a0, a1;
+                unpack2(acc2, a0, a1);
+                l += a0 + a1;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(L::P_FULL + x));
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- epilogue
+            if (!warp_wait(BAR(L::O_FULL + x), it & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + i) * HD;
+#pragma unroll 1
+            for (int q = 0; q < HD / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + q * 32, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                uint32_t pkd[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pkd[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
+                                         __uint_as_float(o[2 * e + 1]) * inv_l);
+                if (i < p.n) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(L::O_EMPTY + x));
+            if (p.lse != nullptr && i < p.n)
+                p.lse[static_cast<size_t>(b * p.H + h) * p.n + i] =
+                    (m + log2f(l)) * 0.69314718055994530942f;
+        }
+    }
+#undef BAR
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------------
 // One-tile self-test of the operand encodings (no counterpart on the pages).
 // ------------------------------------------------------------------------
 __global__ void __launch_bounds__(128, 1)
@@ -647,6 +1079,22 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     p.lse = lse;
     p.status = status_ptr();
     if (p.status == nullptr) return SWA_ERR_CUDA;
+    if (p.G % 2 == 0 && std::getenv("SWA_PREFILL_SINGLE") == nullptr) {
+        // two heads of a GQA pair per work item
+        using L2 = Layout2<HD>;
+        static std::once_flag attr2_once;
+        static cudaError_t attr2_err = cudaSuccess;
+        std::call_once(attr2_once, [] {
+            attr2_err = cudaFuncSetAttribute(swa_prefill_bf16_pair_sm103<HD>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             L2::DYN_SMEM);
+        });
+        if (attr2_err != cudaSuccess) return SWA_ERR_CUDA;
+        p.num_items = B * Hkv * p.n_qt * (p.G / 2);
+        const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
+        swa_prefill_bf16_pair_sm103<HD><<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, p);
+        return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+    }
     const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
     swa_prefill_bf16_sm103<HD><<<grid, NTHREADS, L::DYN_SMEM, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
