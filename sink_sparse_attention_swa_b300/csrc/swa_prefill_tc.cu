@@ -489,13 +489,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // take turns with the tensor core; the MMA warp issues, per key tile c,
 //     P_A(c-1) V, S_A(c) = Q_A K^T, P_B(c-1) V, S_B(c) = Q_B K^T
 // so softmax A(c) runs while the tensor core computes P_B(c-1) V and S_B(c),
-// and the other way round.  TMEM (512 columns): O_A [0,128), S_A [128,256),
+// and the other way round.  384 threads in three warpgroups: warpgroup 0 holds
+// the TMA warp (0) and the MMA warp (1) and gives registers away (setmaxnreg
+// down to 56), the softmax warpgroups 1 (warps 4-7, head A) and 2 (warps 8-11,
+// head B) take them (up to 224), so a full 128-column S row stays in registers.  TMEM (512 columns): O_A [0,128), S_A [128,256),
 // O_B [256,384), S_B [384,512); P (bf16) is written back over the first half
 // of its S buffer.  A tcgen05.commit tracks every MMA issued before it, so the
 // S_X(c) barrier also tells softmax X that P_X(c-1) V has landed in O_X and
 // that O_X may be rescaled.
 // ------------------------------------------------------------------------
-constexpr int NTHREADS2 = 320;
+constexpr int NTHREADS2 = 384;
+// registers per thread after the hand-over: 128 * (56 + 224 + 224) equals the
+// 384 * 168 registers the kernel is launched with
+constexpr int REGS_CTRL = 88;
+constexpr int REGS_SOFTMAX = 208;
 
 template <int HD>
 struct Layout2 {
@@ -635,6 +642,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -777,9 +786,11 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             tc_commit(BAR(L::DRAIN));
             mbar_wait(BAR(L::DRAIN), 0, nullptr, nullptr, TIMEOUT_NS);
         }
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));
         // ------------------------------------------------------------ softmax A / B
-        const int x = (warp - 2) >> 2;           // 0: head h0 (warps 2-5), 1: h0+1 (warps 6-9)
+        const int x = (warp >> 2) - 1;           // 0: head h0 (warps 4-7), 1: h0+1 (warps 8-11)
         const int sub = warp & 3;                // TMEM lane quarter this warp may access
         const int r = sub * 32 + lane;           // query row within the tile
         const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
