@@ -101,9 +101,13 @@ int swa_prefill_ex(const void *Q, const void *K, const void *V, void *O, float *
  * not yet written (pos < w-1) and sink slots of positions still inside the
  * window are not read.
  *   q [B][H][d], Kcache, Vcache [B][Hkv][w+g][d], O [B][H][d]: bf16, device.
- * Split-K over the cached keys, then a log-sum-exp merge; uses a library-owned
- * workspace that grows on demand (cudaMalloc on first use of a size, so make
- * the first call outside stream capture).
+ * Split-K over the cached keys, then a log-sum-exp merge: a first kernel cuts
+ * the cache rows of all (sequence, kv head) pairs, laid end to end, into equal
+ * contiguous shares, one per CTA of a single resident wave, and writes one
+ * partial (max, sum, unnormalised output) per share and pair; a second kernel
+ * merges them.  Uses a library-owned workspace that grows on demand
+ * (cudaMalloc on first use of a size, so make the first call outside stream
+ * capture).
  */
 int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos,
                int B, int H, int Hkv, int d, int w, int g, float scale, void *O,
@@ -115,10 +119,11 @@ size_t swa_decode_workspace_bytes(int B, int H, int Hkv, int d, int w, int g, in
 
 /*
  * swa_decode_ex -- as swa_decode with the element type `dtype`, an optional
- * lse [B][H] fp32 output (NULL to skip), an explicit split count `num_splits`
- * (0 = automatic; 1..1024) and a caller-owned device workspace of
- * `workspace_bytes` >= swa_decode_workspace_bytes(...) (16-byte aligned).
- * Nothing is allocated.
+ * lse [B][H] fp32 output (NULL to skip), a split count `num_splits` (0 =
+ * automatic, one resident wave of CTAs; n in 1..1024 = n*B*Hkv CTAs, about n
+ * shares per (sequence, kv head)) and a caller-owned device workspace of
+ * `workspace_bytes` >= swa_decode_workspace_bytes(...) (16-byte aligned; its
+ * contents need no initialisation).  Nothing is allocated.
  */
 int swa_decode_ex(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos,
                   int B, int H, int Hkv, int d, int w, int g, float scale, void *O,

@@ -65,8 +65,7 @@ int swa_prefill(const void *Q, const void *K, const void *V, void *O, int B, int
 size_t swa_decode_workspace_bytes(int B, int H, int Hkv, int d, int w, int g, int num_splits)
 {
     if (check_heads(B, H, Hkv, d, w, g) != SWA_OK || num_splits < 0 || num_splits > 1024) return 0;
-    const int s = num_splits == 0 ? choose_decode_splits(B, Hkv, w, g) : num_splits;
-    return decode_workspace_bytes(B, H, d, s);
+    return decode_workspace_bytes(B, H, Hkv, d, decode_ctas(B, Hkv, w, g, num_splits));
 }
 
 int swa_decode_ex(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos, int B,
@@ -84,11 +83,11 @@ int swa_decode_ex(const void *q, const void *Kcache, const void *Vcache, const i
         pos == nullptr || (reinterpret_cast<uintptr_t>(pos) & 3u))
         return SWA_ERR_INVALID_ARG;
     if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
-    const int s = num_splits == 0 ? choose_decode_splits(B, Hkv, w, g) : num_splits;
-    const size_t need = decode_workspace_bytes(B, H, d, s);
-    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    const int ctas = decode_ctas(B, Hkv, w, g, num_splits);
+    const size_t need = decode_workspace_bytes(B, H, Hkv, d, ctas);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
         return SWA_ERR_WORKSPACE;
-    return launch_decode(q, Kcache, Vcache, pos, B, H, Hkv, d, w, g, scale, O, lse, dtype, s,
+    return launch_decode(q, Kcache, Vcache, pos, B, H, Hkv, d, w, g, scale, O, lse, dtype, ctas,
                          workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -97,10 +96,9 @@ int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int3
 {
     int rc = check_heads(B, H, Hkv, d, w, g);
     if (rc != SWA_OK) return rc;
-    const int s = choose_decode_splits(B, Hkv, w, g);
-    const size_t need = decode_workspace_bytes(B, H, d, s);
+    const size_t need = decode_workspace_bytes(B, H, Hkv, d, decode_ctas(B, Hkv, w, g, 0));
     void *ws = nullptr;
-    if (need > 0) {
+    {
         int dev = -1;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SWA_ERR_CUDA;
         std::lock_guard<std::mutex> lk(g_ws_mu);
@@ -121,7 +119,7 @@ int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int3
         }
         ws = W.ptr;
     }
-    return swa_decode_ex(q, Kcache, Vcache, pos, B, H, Hkv, d, w, g, scale, O, nullptr, SWA_BF16, s,
+    return swa_decode_ex(q, Kcache, Vcache, pos, B, H, Hkv, d, w, g, scale, O, nullptr, SWA_BF16, 0,
                          ws, need, stream);
 }
 

@@ -85,11 +85,13 @@ int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, fl
 int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
                        int B, int H, int Hkv, int n, int d, int w, int g, float scale,
                        cudaStream_t stream);
-int choose_decode_splits(int B, int Hkv, int w, int g);
-size_t decode_workspace_bytes(int B, int H, int d, int splits);
+// CTAs of the decode split pass: num_splits > 0 asks for about that many per
+// (sequence, kv head); 0 picks one resident wave on the current device.
+int decode_ctas(int B, int Hkv, int w, int g, int num_splits);
+size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int ctas);
 int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *pos, int B,
                   int H, int Hkv, int d, int w, int g, float scale, void *O, float *lse,
-                  swa_dtype dt, int splits, void *ws, cudaStream_t stream);
+                  swa_dtype dt, int ctas, void *ws, cudaStream_t stream);
 int launch_cache_append(void *Kc, void *Vc, const void *kn, const void *vn, const int32_t *pos0,
                         int T, int B, int Hkv, int d, int w, int g, swa_dtype dt,
                         cudaStream_t stream);

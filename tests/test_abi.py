@@ -107,8 +107,12 @@ def test_host_validation_rejects_before_launch(swa):
                            None, 0, None) == -1
     assert L.swa_decode_ex(FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 128, 8, 0, 0.1, FAKE, None, 0, 4,
                            None, 0, None) == -6
-    assert L.swa_decode_workspace_bytes(2, 4, 2, 128, 8, 0, 4) == 2 * 4 * 4 * 130 * 4
-    assert L.swa_decode_workspace_bytes(2, 4, 2, 128, 8, 0, 1) == 0
+    # one partial (m, l, o[d]) per head of the group for each of the
+    # num_splits*B*Hkv CTAs plus one per (sequence, kv head) segment boundary
+    assert L.swa_decode_workspace_bytes(2, 4, 2, 128, 8, 0, 4) == (16 + 4) * 2 * 130 * 4
+    assert L.swa_decode_workspace_bytes(2, 4, 2, 128, 8, 0, 1) == (4 + 4) * 2 * 130 * 4
+    # more CTAs than cache rows are not used: at most one row per CTA
+    assert L.swa_decode_workspace_bytes(1, 2, 1, 64, 3, 1, 1000) == (4 + 1) * 2 * 66 * 4
     # append: negative T, misaligned cache; T == 0 is a no-op
     assert L.swa_cache_append(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 1, 2, 128, 8, 0, 0, None) == -1
     assert L.swa_cache_append(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 1, 1, 2, 128, 8, 0, 0, None) == -1

@@ -48,8 +48,8 @@ def test_noalloc_decode_matches_swa_decode_twice(swa):
 
 @pytest.mark.gpu
 def test_noalloc_rejects_sizes_beyond_the_array(swa):
-    # 64 sequences x 64 heads x 3 splits x (128+2) fp32 = 6.4 MB > 4 MiB
-    B, H, Hkv, d, w, g = 64, 64, 8, 128, 65536, 0
+    # 256 sequences x 8 kv heads: at least 2048 partials x 8 heads x (128+2) fp32 = 8.5 MB > 4 MiB
+    B, H, Hkv, d, w, g = 256, 64, 8, 128, 65536, 0
     need = swa.decode_workspace_bytes(B, H, Hkv, d, w, g)
     assert need > (4 << 20)
     dummy = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
