@@ -10,8 +10,9 @@ in the same run on the streaming-decode workload (B=32, H=32, Hkv=8, d=128,
 w=4096, g=4, pos=100000): one cache append plus one decode per step, reported
 as HBM GB/s over the algorithmic bytes (each cached K/V row read once).
 
-Timing: W warm-up steps, then K timed steps; L2 is flushed (a 256 MiB write)
-before every timed launch and each launch is bracketed by CUDA events on the
+Timing: W warm-up steps, then K timed steps; L2 is flushed (a 256 MiB write,
+then a 256 MiB read, so the flush's dirty lines are written back before the
+timed region) before every timed launch and each launch is bracketed by CUDA events on the
 launching stream.  Under torchrun every rank runs its own replica (weak
 scaling); rank 0 prints one JSON line with the max time over ranks.
 
@@ -225,6 +226,23 @@ def cpu_oracle_sample(min_seconds=10.0, max_seconds=30.0, seed=0, c=None):
 
 
 # --------------------------------------------------------------------------- GPU legs
+class L2Flush:
+    """Evicts L2 before a timed launch and leaves it clean: a 256 MiB write
+    (larger than the 126 MB L2), then a 256 MiB read of a second buffer, so the
+    dirty lines of the write are written back before the timed region starts
+    instead of during it."""
+
+    def __init__(self, device):
+        n = 64 * 1024 * 1024  # 256 MiB of fp32
+        self.w = torch.zeros(n, dtype=torch.float32, device=device)
+        self.r = torch.ones(n, dtype=torch.float32, device=device)
+        self.out = torch.zeros((), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.add_(1)
+        torch.sum(self.r, dim=0, out=self.out)
+
+
 def time_launches(fn, steps, warmup, flush, stream):
     for _ in range(warmup):
         fn()
@@ -232,7 +250,7 @@ def time_launches(fn, steps, warmup, flush, stream):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for k in range(steps):
-        flush.add_(1)  # evict L2 before each timed launch
+        flush()  # evict L2 (clean) before each timed launch
         starts[k].record(stream)
         fn()
         ends[k].record(stream)
@@ -250,9 +268,9 @@ def run_swa(args):
     stream = torch.cuda.current_stream(dev)
     pk = peaks()
     c = PREFILL_WORKLOADS[args.workload]
-    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MiB > L2
+    flush = L2Flush(dev)
     flops = prefill_flops(c)
-    ms = value = achieved = traffic = None
+    ms = value = achieved = traffic = kernel = None
     clk_summary = None
     e2e = None
     if args.only in ("all", "prefill"):
@@ -271,7 +289,9 @@ def run_swa(args):
         value = flops * world / (ms * 1e-3) / 1e12
         launch_ms = float(np.mean(times))
         achieved = flops / (launch_ms * 1e-3) / 1e12
-        traffic = recorded_traffic("swa_prefill_bf16_sm103", args.workload, PREFILL_KERNEL_SRC)
+        kernel = ("swa_prefill_bf16_pair_sm103" if (c["H"] // c["Hkv"]) % 2 == 0
+                  else "swa_prefill_bf16_sm103")
+        traffic = recorded_traffic(kernel, args.workload, PREFILL_KERNEL_SRC)
 
         if not args.no_e2e:
             # ---- end to end through the public API with host buffers
@@ -326,7 +346,7 @@ def run_swa(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": args.workload, **c, "scale": "1/sqrt(d)",
-                   "l2": "flushed before each timed launch (256 MiB write)",
+                   "l2": "flushed before each timed launch: 256 MiB write, then 256 MiB read (L2 left clean)",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "clocks": clk_summary,
         "e2e": e2e,
@@ -334,7 +354,7 @@ def run_swa(args):
         "roofline": None if value is None else {
             "bound": "tensor", "achieved": achieved, "peak": pk["bf16"],
             "unit": "TFLOP/s", "frac": achieved / pk["bf16"], "traffic": traffic,
-            "kernel": "swa_prefill_bf16_sm103", "peak_source": pk["src"] + " burst",
+            "kernel": kernel, "peak_source": pk["src"] + " burst",
             "frac_of_sustained": achieved / pk["bf16_sustained"],
             "useful_flops_per_launch": flops},
         "cpu_baseline": cpu,
