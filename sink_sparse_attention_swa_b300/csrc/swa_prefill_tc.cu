@@ -34,6 +34,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <type_traits>
 
 #include "swa_internal.h"
 #include "swa_ptx.cuh"
@@ -701,6 +702,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // The issuing thread shares its SM sub-partition with two softmax warps,
+        // so its path is kept short: every shared-memory descriptor is a base
+        // computed once plus a compile-time offset, and the K-steps are unrolled.
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(128, BN, 0);
             const uint32_t idesc_o = idesc_bf16_f32(128, HD, 1);
@@ -710,7 +714,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             int prev_st = 0, prev_c = 0, prev_it = 0;
             uint32_t prev_ph = 0;
             // P_X(prev) V into O_X
-            auto issue_pv = [&](int x) -> bool {
+            auto issue_pv = [&](auto xc) -> bool {
+                constexpr int x = decltype(xc)::value;
                 if (!mbar_wait(BAR(L::P_FULL + x), prev_c & 1, abort_flag, p.status, TIMEOUT_NS))
                     return false;
                 if (x == 0 &&
@@ -720,30 +725,34 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                                              p.status, TIMEOUT_NS))
                     return false;
                 tc_fence_after();
-                const uint32_t vbase = sV + prev_st * L::KB;
-                const uint32_t o_col = x * 256, p_col = x * 256 + 128;
-                for (int ks = 0; ks < BN / 16; ++ks) {
-                    const uint64_t bdesc = smem_desc_sw128(vbase + ks * (16 * 128), BN * 128, 1024);
-                    mma_ts(tmem + o_col, tmem + p_col + ks * 8, bdesc, idesc_o,
-                           (!prev_first || ks > 0) ? 1u : 0u);
-                }
+                const uint64_t vb = smem_desc_sw128(sV + prev_st * L::KB, BN * 128, 1024);
+                const uint32_t o_t = tmem + x * 256, p_t = tmem + x * 256 + 128;
+                mma_ts(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
+#pragma unroll
+                for (int ks = 1; ks < BN / 16; ++ks)
+                    mma_ts(o_t, p_t + ks * 8, vb + static_cast<uint64_t>((ks * 16 * 128) >> 4), idesc_o,
+                           1u);
                 if (x == 1) tc_commit(BAR(L::KV_EMPTY + prev_st));
                 if (prev_last) tc_commit(BAR(L::O_FULL + x));
                 return true;
             };
-            auto issue_s = [&](int x, int st, bool last) {
-                const uint32_t qbase = sQ + x * L::QB, kbase = sK + st * L::KB;
+            // S_X = Q_X K^T
+            auto issue_s = [&](auto xc, int st, bool last) {
+                constexpr int x = decltype(xc)::value;
+                const uint64_t qb = smem_desc_sw128(sQ + x * L::QB, 16, 1024);
+                const uint64_t kb = smem_desc_sw128(sK + st * L::KB, 16, 1024);
+                const uint32_t s_t = tmem + x * 256 + 128;
+#pragma unroll
                 for (int ks = 0; ks < HD / 16; ++ks) {
-                    const uint32_t blk = ks >> 2, sub = ks & 3;
-                    const uint64_t adesc =
-                        smem_desc_sw128(qbase + blk * (BM * 128) + sub * 32, 16, 1024);
-                    const uint64_t bdesc =
-                        smem_desc_sw128(kbase + blk * (BN * 128) + sub * 32, 16, 1024);
-                    mma_ss(tmem + x * 256 + 128, adesc, bdesc, idesc_s, ks > 0 ? 1u : 0u);
+                    const uint32_t qo = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
+                    const uint32_t ko = ((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4;
+                    mma_ss(s_t, qb + qo, kb + ko, idesc_s, ks > 0 ? 1u : 0u);
                 }
                 tc_commit(BAR(L::S_FULL + x));
                 if (last) tc_commit(BAR(L::Q_EMPTY + x));
             };
+            using X0 = std::integral_constant<int, 0>;
+            using X1 = std::integral_constant<int, 1>;
             for (int t = blockIdx.x; ok && t < pairs_per_item_count; t += gridDim.x, ++it) {
                 int b, h0, kvh, qt;
                 decode_pair_item(t, p, b, h0, kvh, qt);
@@ -752,25 +761,31 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
                     const bool last = (j == tr.count - 1);
-                    for (int x = 0; x < 2; ++x) {
-                        if (have_prev && !issue_pv(x)) {
-                            ok = false;
-                            break;
-                        }
-                        if (j == 0 && !mbar_wait(BAR(L::Q_FULL + x), it & 1, abort_flag, p.status,
-                                                 TIMEOUT_NS)) {
-                            ok = false;
-                            break;
-                        }
-                        if (x == 0 && !mbar_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status,
-                                                 TIMEOUT_NS)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_s(x, st, last);
+                    // head A: P_A(c-1) V, then S_A(c)
+                    if (have_prev && !issue_pv(X0{})) {
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
+                    if ((j == 0 && !mbar_wait(BAR(L::Q_FULL + 0), it & 1, abort_flag, p.status,
+                                              TIMEOUT_NS)) ||
+                        !mbar_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(X0{}, st, last);
+                    // head B: P_B(c-1) V, then S_B(c)
+                    if (have_prev && !issue_pv(X1{})) {
+                        ok = false;
+                        break;
+                    }
+                    if (j == 0 && !mbar_wait(BAR(L::Q_FULL + 1), it & 1, abort_flag, p.status,
+                                             TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(X1{}, st, last);
                     have_prev = true;
                     prev_st = st;
                     prev_ph = ph;
@@ -781,7 +796,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 }
             }
             if (ok && have_prev) {
-                if (issue_pv(0)) issue_pv(1);
+                if (issue_pv(X0{})) issue_pv(X1{});
             }
             tc_commit(BAR(L::DRAIN));
             mbar_wait(BAR(L::DRAIN), 0, nullptr, nullptr, TIMEOUT_NS);
