@@ -531,16 +531,30 @@ struct Layout2 {
     static constexpr uint32_t DYN_SMEM = (BYTES + 1024 > 120 * 1024) ? BYTES + 1024 : 120 * 1024;
 };
 
-__device__ __forceinline__ void decode_pair_item(int t, const PrefillParams &p, int &b, int &h0,
+// Work order of the pair kernel.  Items are ranked q tile first, the last q
+// tile (the most key tiles) first; within a q tile by sequence, kv head and
+// head pair, so the CTAs working at the same time share one band position of
+// every kv head (a few MB of K/V in L2).  Rank r goes to CTA r % P in even
+// rounds and P-1 - r % P in odd rounds (a snake), which evens out the cheaper
+// q tiles at the start of the sequence across the CTAs.  CTA c's k-th item has
+// rank pair_item_rank(c, k); ranks >= num_items end its loop.
+__device__ __forceinline__ int pair_item_rank(int c, int k)
+{
+    const int P = static_cast<int>(gridDim.x);
+    return k * P + ((k & 1) ? P - 1 - c : c);
+}
+
+__device__ __forceinline__ void decode_pair_item(int r, const PrefillParams &p, int &b, int &h0,
                                                  int &kvh, int &qt)
 {
     const int pairs = p.G >> 1;
-    const int hp = t % pairs;
-    t /= pairs;
-    qt = t % p.n_qt;
-    t /= p.n_qt;
-    kvh = t % p.Hkv;
-    b = t / p.Hkv;
+    const int per_qt = p.B * p.Hkv * pairs;
+    qt = p.n_qt - 1 - r / per_qt;
+    r %= per_qt;
+    const int hp = r % pairs;
+    r /= pairs;
+    kvh = r % p.Hkv;
+    b = r / p.Hkv;
     h0 = kvh * p.G + 2 * hp;
 }
 
@@ -652,7 +666,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             int last_k_par[STAGES], last_q_par[2] = {-1, -1};
             for (int s = 0; s < STAGES; ++s) last_k_par[s] = -1;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < pairs_per_item_count; t += gridDim.x, ++it) {
+            for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
+                 t = pair_item_rank(blockIdx.x, ++it)) {
                 int b, h0, kvh, qt;
                 decode_pair_item(t, p, b, h0, kvh, qt);
                 const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
@@ -678,23 +693,22 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     }
                     const int k0 = tile_kt(tr, j) * BN;
                     const int zkv = b * p.Hkv + kvh;
-                    mbar_expect_tx(BAR(L::K_FULL + st), L::KB);
+                    // K and V of a stage complete one barrier: the MMA issuer waits
+                    // once per key tile
+                    mbar_expect_tx(BAR(L::K_FULL + st), 2 * L::KB);
                     for (int c = 0; c < HD / 64; ++c)
                         tma_load_3d(sK + st * L::KB + c * (BN * 128), &tmK, BAR(L::K_FULL + st),
                                     c * 64, k0, zkv);
-                    mbar_expect_tx(BAR(L::V_FULL + st), L::KB);
                     for (int c = 0; c < HD / 64; ++c)
-                        tma_load_3d(sV + st * L::KB + c * (BN * 128), &tmV, BAR(L::V_FULL + st),
+                        tma_load_3d(sV + st * L::KB + c * (BN * 128), &tmV, BAR(L::K_FULL + st),
                                     c * 64, k0, zkv);
                     last_k_par[st] = static_cast<int>(ph);
                 }
             }
             if (!ok) {
                 for (int s = 0; s < STAGES; ++s)
-                    if (last_k_par[s] >= 0) {
+                    if (last_k_par[s] >= 0)
                         mbar_wait(BAR(L::K_FULL + s), last_k_par[s], nullptr, nullptr, TIMEOUT_NS);
-                        mbar_wait(BAR(L::V_FULL + s), last_k_par[s], nullptr, nullptr, TIMEOUT_NS);
-                    }
                 for (int x = 0; x < 2; ++x)
                     if (last_q_par[x] >= 0)
                         mbar_wait(BAR(L::Q_FULL + x), last_q_par[x], nullptr, nullptr, TIMEOUT_NS);
@@ -712,14 +726,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             bool ok = true;
             bool have_prev = false, prev_first = false, prev_last = false;
             int prev_st = 0, prev_c = 0, prev_it = 0;
-            uint32_t prev_ph = 0;
             // P_X(prev) V into O_X
             auto issue_pv = [&](auto xc) -> bool {
                 constexpr int x = decltype(xc)::value;
                 if (!mbar_wait(BAR(L::P_FULL + x), prev_c & 1, abort_flag, p.status, TIMEOUT_NS))
-                    return false;
-                if (x == 0 &&
-                    !mbar_wait(BAR(L::V_FULL + prev_st), prev_ph, abort_flag, p.status, TIMEOUT_NS))
                     return false;
                 if (prev_first && !mbar_wait(BAR(L::O_EMPTY + x), (prev_it & 1) ^ 1, abort_flag,
                                              p.status, TIMEOUT_NS))
@@ -753,7 +763,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             };
             using X0 = std::integral_constant<int, 0>;
             using X1 = std::integral_constant<int, 1>;
-            for (int t = blockIdx.x; ok && t < pairs_per_item_count; t += gridDim.x, ++it) {
+            for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
+                 t = pair_item_rank(blockIdx.x, ++it)) {
                 int b, h0, kvh, qt;
                 decode_pair_item(t, p, b, h0, kvh, qt);
                 const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
@@ -788,7 +799,6 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     issue_s(X1{}, st, last);
                     have_prev = true;
                     prev_st = st;
-                    prev_ph = ph;
                     prev_c = c;
                     prev_it = it;
                     prev_first = (j == 0);
@@ -815,7 +825,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         const uint64_t sl2x2 = pack2(__float_as_uint(sl2), __float_as_uint(sl2));
         int c = 0, it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < pairs_per_item_count; t += gridDim.x, ++it) {
+        for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
+                 t = pair_item_rank(blockIdx.x, ++it)) {
             int b, h0, kvh, qt;
             decode_pair_item(t, p, b, h0, kvh, qt);
             const int h = h0 + x;
