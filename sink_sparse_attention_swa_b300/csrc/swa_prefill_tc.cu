@@ -716,10 +716,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // The issuing thread shares its SM sub-partition with two softmax warps,
-        // so its path is kept short: every shared-memory descriptor is a base
-        // computed once plus a compile-time offset, and the K-steps are unrolled.
-        if (lane == 0) {
+        // The issuing warp shares its SM sub-partition with two softmax warps,
+        // and a single thread issues a 128x128x16 MMA only a little faster than
+        // the tensor core executes it, so the issue path is kept short: the
+        // whole warp runs the loop (waits, bookkeeping) and each MMA and commit
+        // is issued by one elected lane; descriptor bases are computed once per
+        // group and the K-steps are unrolled with compile-time offsets.
+        {
             const uint32_t idesc_s = idesc_bf16_f32(128, BN, 0);
             const uint32_t idesc_o = idesc_bf16_f32(128, HD, 1);
             int kv_iter = 0, it = 0, c = 0;
@@ -729,21 +732,21 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             // P_X(prev) V into O_X
             auto issue_pv = [&](auto xc) -> bool {
                 constexpr int x = decltype(xc)::value;
-                if (!mbar_wait(BAR(L::P_FULL + x), prev_c & 1, abort_flag, p.status, TIMEOUT_NS))
+                if (!warp_wait(BAR(L::P_FULL + x), prev_c & 1, abort_flag, p.status))
                     return false;
-                if (prev_first && !mbar_wait(BAR(L::O_EMPTY + x), (prev_it & 1) ^ 1, abort_flag,
-                                             p.status, TIMEOUT_NS))
+                if (prev_first && !warp_wait(BAR(L::O_EMPTY + x), (prev_it & 1) ^ 1, abort_flag,
+                                             p.status))
                     return false;
                 tc_fence_after();
                 const uint64_t vb = smem_desc_sw128(sV + prev_st * L::KB, BN * 128, 1024);
                 const uint32_t o_t = tmem + x * 256, p_t = tmem + x * 256 + 128;
-                mma_ts(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
+                mma_ts_e(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
 #pragma unroll
                 for (int ks = 1; ks < BN / 16; ++ks)
-                    mma_ts(o_t, p_t + ks * 8, vb + static_cast<uint64_t>((ks * 16 * 128) >> 4), idesc_o,
-                           1u);
-                if (x == 1) tc_commit(BAR(L::KV_EMPTY + prev_st));
-                if (prev_last) tc_commit(BAR(L::O_FULL + x));
+                    mma_ts_e(o_t, p_t + ks * 8, vb + static_cast<uint64_t>((ks * 16 * 128) >> 4),
+                             idesc_o, 1u);
+                if (x == 1) tc_commit_e(BAR(L::KV_EMPTY + prev_st));
+                if (prev_last) tc_commit_e(BAR(L::O_FULL + x));
                 return true;
             };
             // S_X = Q_X K^T
@@ -756,10 +759,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 for (int ks = 0; ks < HD / 16; ++ks) {
                     const uint32_t qo = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
                     const uint32_t ko = ((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4;
-                    mma_ss(s_t, qb + qo, kb + ko, idesc_s, ks > 0 ? 1u : 0u);
+                    mma_ss_e(s_t, qb + qo, kb + ko, idesc_s, ks > 0 ? 1u : 0u);
                 }
-                tc_commit(BAR(L::S_FULL + x));
-                if (last) tc_commit(BAR(L::Q_EMPTY + x));
+                tc_commit_e(BAR(L::S_FULL + x));
+                if (last) tc_commit_e(BAR(L::Q_EMPTY + x));
             };
             using X0 = std::integral_constant<int, 0>;
             using X1 = std::integral_constant<int, 1>;
@@ -777,9 +780,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         ok = false;
                         break;
                     }
-                    if ((j == 0 && !mbar_wait(BAR(L::Q_FULL + 0), it & 1, abort_flag, p.status,
-                                              TIMEOUT_NS)) ||
-                        !mbar_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, TIMEOUT_NS)) {
+                    if ((j == 0 && !warp_wait(BAR(L::Q_FULL + 0), it & 1, abort_flag, p.status)) ||
+                        !warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -790,8 +792,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         ok = false;
                         break;
                     }
-                    if (j == 0 && !mbar_wait(BAR(L::Q_FULL + 1), it & 1, abort_flag, p.status,
-                                             TIMEOUT_NS)) {
+                    if (j == 0 && !warp_wait(BAR(L::Q_FULL + 1), it & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -808,8 +809,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             if (ok && have_prev) {
                 if (issue_pv(X0{})) issue_pv(X1{});
             }
-            tc_commit(BAR(L::DRAIN));
-            mbar_wait(BAR(L::DRAIN), 0, nullptr, nullptr, TIMEOUT_NS);
+            // drain: every MMA this warp issued has completed before exit
+            tc_commit_e(BAR(L::DRAIN));
+            warp_wait(BAR(L::DRAIN), 0, nullptr, nullptr);
         }
     }
     } else {
