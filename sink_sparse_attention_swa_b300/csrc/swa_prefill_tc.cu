@@ -239,7 +239,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop; each MMA and commit is issued by one
+        // elected lane, with descriptor bases computed once per group.
+        {
             const uint32_t idesc_s = idesc_bf16_f32(128, BN, 0);
             const uint32_t idesc_o = idesc_bf16_f32(128, HD, 1);
             int kv_iter = 0, it = 0, c = 0;
@@ -251,23 +253,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bool prev_first = false;
             auto issue_pv = [&]() -> bool {
                 const int pb = prev_c & 1;
-                if (!mbar_wait(BAR(L::P_FULL + pb), (prev_c >> 1) & 1, abort_flag, p.status,
-                               TIMEOUT_NS))
+                if (!warp_wait(BAR(L::P_FULL + pb), (prev_c >> 1) & 1, abort_flag, p.status))
                     return false;
-                if (!mbar_wait(BAR(L::V_FULL + prev_st), prev_ph, abort_flag, p.status, TIMEOUT_NS))
+                if (!warp_wait(BAR(L::V_FULL + prev_st), prev_ph, abort_flag, p.status))
                     return false;
-                if (prev_first && !mbar_wait(BAR(L::O_EMPTY), (prev_it & 1) ^ 1, abort_flag,
-                                             p.status, TIMEOUT_NS))
+                if (prev_first &&
+                    !warp_wait(BAR(L::O_EMPTY), (prev_it & 1) ^ 1, abort_flag, p.status))
                     return false;
                 tc_fence_after();
-                const uint32_t vbase = sV + prev_st * L::KB;
-                for (int ks = 0; ks < BN / 16; ++ks) {
-                    const uint64_t bdesc = smem_desc_sw128(vbase + ks * (16 * 128), BN * 128, 1024);
-                    mma_ts(tmem, tmem + P_COL0 + pb * (BN / 2) + ks * 8, bdesc, idesc_o,
-                           (!prev_first || ks > 0) ? 1u : 0u);
-                }
-                tc_commit(BAR(L::KV_EMPTY + prev_st));
-                tc_commit(BAR(L::PV_DONE + pb));
+                const uint64_t vb = smem_desc_sw128(sV + prev_st * L::KB, BN * 128, 1024);
+                const uint32_t p_t = tmem + P_COL0 + pb * (BN / 2);
+                mma_ts_e(tmem, p_t, vb, idesc_o, prev_first ? 0u : 1u);
+#pragma unroll
+                for (int ks = 1; ks < BN / 16; ++ks)
+                    mma_ts_e(tmem, p_t + ks * 8, vb + static_cast<uint64_t>((ks * 16 * 128) >> 4),
+                             idesc_o, 1u);
+                tc_commit_e(BAR(L::KV_EMPTY + prev_st));
+                tc_commit_e(BAR(L::PV_DONE + pb));
                 return true;
             };
             for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
@@ -275,8 +277,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 decode_item(t, p, b, h, kvh, qt);
                 const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
                 const int qb = it & 1;
-                if (!mbar_wait(BAR(L::Q_FULL + qb), (it >> 1) & 1, abort_flag, p.status,
-                               TIMEOUT_NS)) {
+                if (!warp_wait(BAR(L::Q_FULL + qb), (it >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -284,24 +285,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
                     const int sbuf = c & 1;
-                    if (!mbar_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, TIMEOUT_NS) ||
-                        !mbar_wait(BAR(L::S_EMPTY + sbuf), ((c >> 1) & 1) ^ 1, abort_flag, p.status,
-                                   TIMEOUT_NS)) {
+                    if (!warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status) ||
+                        !warp_wait(BAR(L::S_EMPTY + sbuf), ((c >> 1) & 1) ^ 1, abort_flag,
+                                   p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t qbase = sQ + qb * L::QB, kbase = sK + st * L::KB;
+                    const uint64_t qd = smem_desc_sw128(sQ + qb * L::QB, 16, 1024);
+                    const uint64_t kd = smem_desc_sw128(sK + st * L::KB, 16, 1024);
+#pragma unroll
                     for (int ks = 0; ks < HD / 16; ++ks) {
-                        const uint32_t blk = ks >> 2, sub = ks & 3;
-                        const uint64_t adesc =
-                            smem_desc_sw128(qbase + blk * (BM * 128) + sub * 32, 16, 1024);
-                        const uint64_t bdesc =
-                            smem_desc_sw128(kbase + blk * (BN * 128) + sub * 32, 16, 1024);
-                        mma_ss(tmem + S_COL0 + sbuf * BN, adesc, bdesc, idesc_s, ks > 0 ? 1u : 0u);
+                        const uint32_t qo = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
+                        const uint32_t ko = ((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4;
+                        mma_ss_e(tmem + S_COL0 + sbuf * BN, qd + qo, kd + ko, idesc_s,
+                                 ks > 0 ? 1u : 0u);
                     }
-                    tc_commit(BAR(L::S_FULL + sbuf));
-                    if (j == tr.count - 1) tc_commit(BAR(L::Q_EMPTY + qb));
+                    tc_commit_e(BAR(L::S_FULL + sbuf));
+                    if (j == tr.count - 1) tc_commit_e(BAR(L::Q_EMPTY + qb));
                     if (have_prev && !issue_pv()) {
                         ok = false;
                         break;
@@ -315,9 +316,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             if (ok && have_prev) issue_pv();
-            // drain: every MMA this thread issued has completed before exit
-            tc_commit(BAR(L::DRAIN));
-            mbar_wait(BAR(L::DRAIN), 0, nullptr, nullptr, TIMEOUT_NS);
+            // drain: every MMA this warp issued has completed before exit
+            tc_commit_e(BAR(L::DRAIN));
+            warp_wait(BAR(L::DRAIN), 0, nullptr, nullptr);
         }
     } else {
         // ------------------------------------------------------------ softmax
