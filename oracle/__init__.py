@@ -55,11 +55,12 @@ def _load():
         lib.oracle_count_pairs.argtypes = [_i64, _i64, _i64]
         lib.oracle_count_pairs.restype = _i64
         lib.oracle_tiles.argtypes = [_i64, _i64, _i64, _i64, _i64, _ptr]
-        lib.oracle_prefill.argtypes = [_ptr] * 5 + [_i64] * 7 + [_dbl, ctypes.c_int]
-        lib.oracle_prefill_rows.argtypes = [_ptr] * 3 + [_i64] * 7 + [_dbl, _ptr, _i64, _ptr, _ptr]
-        lib.oracle_decode_history.argtypes = [_ptr] * 4 + [_i64] * 7 + [_dbl, _ptr, _ptr]
+        lib.oracle_prefill.argtypes = [_ptr] * 5 + [_i64] * 7 + [_dbl, ctypes.c_int, _ptr]
+        lib.oracle_prefill_rows.argtypes = [_ptr] * 3 + [_i64] * 7 + [_dbl, _ptr, _i64, _ptr, _ptr,
+                                                                    _ptr]
+        lib.oracle_decode_history.argtypes = [_ptr] * 4 + [_i64] * 7 + [_dbl, _ptr, _ptr, _ptr]
         lib.oracle_cache_slots.argtypes = [_i64, _i64, _i64, _ptr, _ptr]
-        lib.oracle_decode_cache.argtypes = [_ptr] * 4 + [_i64] * 6 + [_dbl, _ptr, _ptr]
+        lib.oracle_decode_cache.argtypes = [_ptr] * 4 + [_i64] * 6 + [_dbl, _ptr, _ptr, _ptr]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -75,6 +76,19 @@ def _f64(a) -> np.ndarray:
 
 def _p(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _sinks(sink_logit, H):
+    """Per-head sink logits as float64 [H] (None: no sink logit)."""
+    if sink_logit is None:
+        return None
+    a = _f64(sink_logit).reshape(-1)
+    assert a.shape == (H,), (a.shape, H)
+    return a
+
+
+def _pn(a):
+    return None if a is None else _p(a)
 
 
 def num_threads() -> int:
@@ -110,20 +124,22 @@ def tiles(n: int, w: int, g: int, BM: int, BN: int) -> np.ndarray:
     return out
 
 
-def prefill(Q, K, V, w: int, g: int, scale: float, zero_score: bool = False):
-    """Q [B,H,n,d], K/V [B,Hkv,n,d] -> (O [B,H,n,d], LSE [B,H,n]) in float64."""
+def prefill(Q, K, V, w: int, g: int, scale: float, zero_score: bool = False, sink_logit=None):
+    """Q [B,H,n,d], K/V [B,Hkv,n,d] -> (O [B,H,n,d], LSE [B,H,n]) in float64.
+    sink_logit: optional per-head sink logits [H] (see the C source)."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     B, H, n, d = Q.shape
     Hkv = K.shape[1]
     assert K.shape == (B, Hkv, n, d) and V.shape == K.shape and H % Hkv == 0
     O = np.empty_like(Q)
     L = np.empty((B, H, n), dtype=np.float64)
+    sl = _sinks(sink_logit, H)
     _load().oracle_prefill(_p(Q), _p(K), _p(V), _p(O), _p(L), B, H, Hkv, n, d, w, g,
-                           float(scale), int(bool(zero_score)))
+                           float(scale), int(bool(zero_score)), _pn(sl))
     return O, L
 
 
-def prefill_rows(q_rows, K, V, H: int, w: int, g: int, scale: float, rows):
+def prefill_rows(q_rows, K, V, H: int, w: int, g: int, scale: float, rows, sink_logit=None):
     """Sampled prefill rows.  rows: int array [m,3] of (b, h, i); q_rows [m,d] the
     matching query rows; K/V [B,Hkv,n,d].  Returns (O_rows [m,d], LSE_rows [m])."""
     q_rows, K, V = _f64(q_rows), _f64(K), _f64(V)
@@ -133,12 +149,13 @@ def prefill_rows(q_rows, K, V, H: int, w: int, g: int, scale: float, rows):
     assert rows.shape == (m, 3) and q_rows.shape == (m, d)
     O = np.empty((m, d), dtype=np.float64)
     L = np.empty(m, dtype=np.float64)
+    sl = _sinks(sink_logit, H)
     _load().oracle_prefill_rows(_p(q_rows), _p(K), _p(V), B, H, Hkv, n, d, w, g,
-                                float(scale), _p(rows), m, _p(O), _p(L))
+                                float(scale), _p(rows), m, _p(O), _p(L), _pn(sl))
     return O, L
 
 
-def decode_history(q, Khist, Vhist, pos, w: int, g: int, scale: float):
+def decode_history(q, Khist, Vhist, pos, w: int, g: int, scale: float, sink_logit=None):
     """q [B,H,d]; Khist/Vhist [B,Hkv,P,d] indexed by position; pos [B]."""
     q, Kh, Vh = _f64(q), _f64(Khist), _f64(Vhist)
     pos = np.ascontiguousarray(pos, dtype=np.int64)
@@ -148,8 +165,9 @@ def decode_history(q, Khist, Vhist, pos, w: int, g: int, scale: float):
     assert int(pos.max()) < P
     O = np.empty_like(q)
     L = np.empty((B, H), dtype=np.float64)
+    sl = _sinks(sink_logit, H)
     _load().oracle_decode_history(_p(q), _p(Kh), _p(Vh), _p(pos), P, B, H, Hkv, d, w, g,
-                                  float(scale), _p(O), _p(L))
+                                  float(scale), _p(O), _p(L), _pn(sl))
     return O, L
 
 
@@ -160,7 +178,7 @@ def cache_slots(p: int, w: int, g: int):
     return int(r.value), int(s.value)
 
 
-def decode_cache(q, Kc, Vc, pos, w: int, g: int, scale: float):
+def decode_cache(q, Kc, Vc, pos, w: int, g: int, scale: float, sink_logit=None):
     """q [B,H,d]; Kc/Vc [B,Hkv,w+g,d] rolling cache; pos [B]."""
     q, Kc, Vc = _f64(q), _f64(Kc), _f64(Vc)
     pos = np.ascontiguousarray(pos, dtype=np.int64)
@@ -169,6 +187,7 @@ def decode_cache(q, Kc, Vc, pos, w: int, g: int, scale: float):
     assert Kc.shape == (B, Hkv, w + g, d) and Vc.shape == Kc.shape and pos.shape == (B,)
     O = np.empty_like(q)
     L = np.empty((B, H), dtype=np.float64)
+    sl = _sinks(sink_logit, H)
     _load().oracle_decode_cache(_p(q), _p(Kc), _p(Vc), _p(pos), B, H, Hkv, d, w, g,
-                                float(scale), _p(O), _p(L))
+                                float(scale), _p(O), _p(L), _pn(sl))
     return O, L

@@ -169,13 +169,19 @@ void oracle_tiles(int64_t n, int64_t w, int64_t g, int64_t BM, int64_t BN, int32
  * Softmax in fp64 with the maximum subtracted.  lse = log(sum_j exp(s_j)),
  * natural log ([SW] §6 stage 3 and §10: the log-sum-exp lets results over
  * disjoint key sets be normalised jointly).
+ *
+ * sink_logit: the learned per-head attention sink of [SW] §6 stage 3 (a
+ * logit that absorbs probability mass when nothing is relevant), taken as
+ * one more entry of the softmax with score sink_logit and a value vector of
+ * zeros: it enters the maximum and the normalising sum, not the output.
+ * -INFINITY means no such sink (the plain softmax above).
  */
 static void attend_row(const double *q, const double *K, const double *V,
                        const uint8_t *row, int64_t nkeys, int64_t d, double scale,
-                       int zero_score, double *s, double *o, double *lse)
+                       int zero_score, double sink_logit, double *s, double *o, double *lse)
 {
     int64_t j, k;
-    double mx = -INFINITY, sum = 0.0;
+    double mx = sink_logit, sum = 0.0;
     for (j = 0; j < nkeys; ++j) {
         if (row[j]) {
             double dot = 0.0;
@@ -198,10 +204,17 @@ static void attend_row(const double *q, const double *K, const double *V,
         for (k = 0; k < d; ++k)
             o[k] += p * V[j * d + k];
     }
+    sum += exp(sink_logit - mx); /* the sink: in the sum, value zero */
     for (k = 0; k < d; ++k)
         o[k] /= sum;
     if (lse)
         *lse = mx + log(sum);
+}
+
+/* sink_logits [H] or NULL: the per-head sink logit of query head h. */
+static double sink_of(const double *sink_logits, int64_t h)
+{
+    return sink_logits ? sink_logits[h] : -INFINITY;
 }
 
 /*
@@ -212,7 +225,8 @@ static void attend_row(const double *q, const double *K, const double *V,
  */
 void oracle_prefill(const double *Q, const double *K, const double *V, double *O, double *LSE,
                     int64_t B, int64_t H, int64_t Hkv, int64_t n, int64_t d,
-                    int64_t w, int64_t g, double scale, int zero_score)
+                    int64_t w, int64_t g, double scale, int zero_score,
+                    const double *sink_logits)
 {
     int64_t r, rows = B * H * n, G = H / Hkv;
 #pragma omp parallel
@@ -226,8 +240,8 @@ void oracle_prefill(const double *Q, const double *K, const double *V, double *O
             const double *Kbh = K + ((b * Hkv + kvh) * n) * d;
             const double *Vbh = V + ((b * Hkv + kvh) * n) * d;
             oracle_mask_row(i, n, w, g, mrow);
-            attend_row(Q + r * d, Kbh, Vbh, mrow, n, d, scale, zero_score, s, O + r * d,
-                       LSE ? LSE + r : NULL);
+            attend_row(Q + r * d, Kbh, Vbh, mrow, n, d, scale, zero_score,
+                       sink_of(sink_logits, h), s, O + r * d, LSE ? LSE + r : NULL);
         }
         free(mrow);
         free(s);
@@ -243,7 +257,8 @@ void oracle_prefill(const double *Q, const double *K, const double *V, double *O
 void oracle_prefill_rows(const double *q_rows, const double *K, const double *V,
                          int64_t B, int64_t H, int64_t Hkv, int64_t n, int64_t d,
                          int64_t w, int64_t g, double scale,
-                         const int64_t *rows, int64_t nrows, double *O_rows, double *LSE_rows)
+                         const int64_t *rows, int64_t nrows, double *O_rows, double *LSE_rows,
+                         const double *sink_logits)
 {
     int64_t t, G = H / Hkv;
     (void)B;
@@ -259,8 +274,8 @@ void oracle_prefill_rows(const double *q_rows, const double *K, const double *V,
             const double *Kbh = K + ((b * Hkv + kvh) * n) * d;
             const double *Vbh = V + ((b * Hkv + kvh) * n) * d;
             oracle_mask_row(i, n, w, g, mrow);
-            attend_row(q, Kbh, Vbh, mrow, n, d, scale, 0, s, O_rows + t * d,
-                       LSE_rows ? LSE_rows + t : NULL);
+            attend_row(q, Kbh, Vbh, mrow, n, d, scale, 0, sink_of(sink_logits, h), s,
+                       O_rows + t * d, LSE_rows ? LSE_rows + t : NULL);
         }
         free(mrow);
         free(s);
@@ -283,7 +298,8 @@ void oracle_prefill_rows(const double *q_rows, const double *K, const double *V,
 void oracle_decode_history(const double *q, const double *Khist, const double *Vhist,
                            const int64_t *pos, int64_t P,
                            int64_t B, int64_t H, int64_t Hkv, int64_t d,
-                           int64_t w, int64_t g, double scale, double *O, double *LSE)
+                           int64_t w, int64_t g, double scale, double *O, double *LSE,
+                           const double *sink_logits)
 {
     int64_t r, G = H / Hkv;
 #pragma omp parallel
@@ -296,8 +312,8 @@ void oracle_decode_history(const double *q, const double *Khist, const double *V
             const double *Kbh = Khist + ((b * Hkv + kvh) * P) * d;
             const double *Vbh = Vhist + ((b * Hkv + kvh) * P) * d;
             oracle_mask_row(p, p + 1, w, g, mrow);
-            attend_row(q + r * d, Kbh, Vbh, mrow, p + 1, d, scale, 0, s, O + r * d,
-                       LSE ? LSE + r : NULL);
+            attend_row(q + r * d, Kbh, Vbh, mrow, p + 1, d, scale, 0, sink_of(sink_logits, h), s,
+                       O + r * d, LSE ? LSE + r : NULL);
         }
         free(mrow);
         free(s);
@@ -326,7 +342,8 @@ void oracle_cache_slots(int64_t p, int64_t w, int64_t g, int64_t *ring, int64_t 
  */
 void oracle_decode_cache(const double *q, const double *Kc, const double *Vc,
                          const int64_t *pos, int64_t B, int64_t H, int64_t Hkv, int64_t d,
-                         int64_t w, int64_t g, double scale, double *O, double *LSE)
+                         int64_t w, int64_t g, double scale, double *O, double *LSE,
+                         const double *sink_logits)
 {
     int64_t r, G = H / Hkv, S = w + g;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -358,7 +375,8 @@ void oracle_decode_cache(const double *q, const double *Kc, const double *Vc,
             ones[cnt] = 1;
             ++cnt;
         }
-        attend_row(q + r * d, Kg, Vg, ones, cnt, d, scale, 0, s, O + r * d, LSE ? LSE + r : NULL);
+        attend_row(q + r * d, Kg, Vg, ones, cnt, d, scale, 0, sink_of(sink_logits, h), s, O + r * d,
+                   LSE ? LSE + r : NULL);
         free(mrow);
         free(Kg);
         free(Vg);

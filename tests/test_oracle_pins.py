@@ -341,3 +341,84 @@ def test_streaming_cache_matches_unbounded_history(oracle_mod, w, g):
         Oh, Lh = oracle_mod.decode_history(q[p], K, V, pos, w, g, 0.6)
         assert np.allclose(Oc, Oh, atol=1e-12, rtol=0), p
         assert np.allclose(Lc, Lh, atol=1e-12, rtol=0), p
+
+
+# --------------------------------------------------------------------------
+# learned per-head sink logit ("Sliding Window and Sparse Attention, from
+# Longformer to CSA2", section 6, stage 3): one more softmax entry per head
+# with score sink_h and a zero value vector
+# --------------------------------------------------------------------------
+def sdpa_with_sink(Q, K, V, mask_bool, scale, sink):
+    """torch SDPA over the keys plus one extra zero key/zero value whose
+    additive mask entry is sink[h]; also returns the log-sum-exp."""
+    B, H, n, d = Q.shape
+    G = H // K.shape[1]
+    Ke = torch.cat([K.repeat_interleave(G, dim=1), torch.zeros(B, H, 1, d, dtype=Q.dtype)], dim=2)
+    Ve = torch.cat([V.repeat_interleave(G, dim=1), torch.zeros(B, H, 1, d, dtype=Q.dtype)], dim=2)
+    bias = torch.full((B, H, n, n + 1), -math.inf, dtype=Q.dtype)
+    bias[..., :n][:, :, torch.as_tensor(mask_bool, dtype=torch.bool)] = 0.0
+    bias[..., n] = torch.as_tensor(sink, dtype=Q.dtype).view(1, H, 1)
+    O = torch.nn.functional.scaled_dot_product_attention(Q, Ke, Ve, attn_mask=bias, scale=scale)
+    L = torch.logsumexp(scale * Q @ Ke.transpose(-1, -2) + bias, dim=-1)
+    return O, L
+
+
+@pytest.mark.parametrize("n,w,g,H,Hkv", [(40, 7, 2, 2, 1), (33, 50, 0, 4, 2), (25, 1, 3, 2, 2)])
+def test_sink_logit_is_an_extra_zero_value_entry(oracle_mod, n, w, g, H, Hkv):
+    B, d, scale = 2, 16, 0.3
+    Q, K, V = rand(B, H, n, d, seed=40), rand(B, Hkv, n, d, seed=41), rand(B, Hkv, n, d, seed=42)
+    sink = np.linspace(-2.0, 3.0, H)
+    O, L = oracle_mod.prefill(Q, K, V, w, g, scale, sink_logit=sink)
+    ref, refL = sdpa_with_sink(Q, K, V, torch_mask(n, w, g).astype(bool), scale, sink)
+    assert np.allclose(O, ref.numpy(), atol=1e-12, rtol=0)
+    assert np.allclose(L, refL.numpy(), atol=1e-12, rtol=0)
+
+
+def test_sink_logit_window_one_is_a_sigmoid(oracle_mod):
+    # w = 1: the only key is the row itself, so O_i = V_i * sigmoid(s_ii - sink)
+    B, H, n, d, scale = 1, 3, 20, 8, 0.5
+    Q, K, V = rand(B, H, n, d, seed=43), rand(B, H, n, d, seed=44), rand(B, H, n, d, seed=45)
+    sink = np.array([-1.0, 0.0, 2.5])
+    O, L = oracle_mod.prefill(Q, K, V, 1, 0, scale, sink_logit=sink)
+    s_ii = scale * (Q * K).sum(-1).numpy()
+    sig = 1.0 / (1.0 + np.exp(-(s_ii - sink.reshape(1, H, 1))))
+    assert np.allclose(O, V.numpy() * sig[..., None], atol=1e-13, rtol=0)
+    assert np.allclose(L, np.logaddexp(s_ii, sink.reshape(1, H, 1)), atol=1e-13, rtol=0)
+
+
+def test_sink_logit_minus_inf_and_huge(oracle_mod):
+    B, H, Hkv, n, d = 1, 2, 1, 30, 8
+    Q, K, V = rand(B, H, n, d, seed=46), rand(B, Hkv, n, d, seed=47), rand(B, Hkv, n, d, seed=48)
+    O0, L0 = oracle_mod.prefill(Q, K, V, 6, 2, 0.4)
+    O1, L1 = oracle_mod.prefill(Q, K, V, 6, 2, 0.4, sink_logit=np.full(H, -np.inf))
+    assert np.array_equal(O0, O1) and np.array_equal(L0, L1)  # no sink: the plain softmax
+    O2, L2 = oracle_mod.prefill(Q, K, V, 6, 2, 0.4, sink_logit=np.full(H, 800.0))
+    assert np.abs(O2).max() < 1e-300  # the sink takes all the mass
+    assert np.allclose(L2, 800.0, atol=1e-12, rtol=0)
+
+
+def test_sink_logit_decode_matches_prefill_rows(oracle_mod):
+    B, H, Hkv, d, P, w, g = 2, 4, 2, 16, 30, 6, 2
+    K, V = rand(B, Hkv, P, d, seed=49), rand(B, Hkv, P, d, seed=50)
+    q = rand(B, H, d, seed=51)
+    sink = np.array([0.5, -0.5, 1.5, -3.0])
+    pos = np.array([29, 11])
+    Oh, Lh = oracle_mod.decode_history(q, K, V, pos, w, g, 0.25, sink_logit=sink)
+    for b in range(B):
+        p = int(pos[b])
+        Q = torch.zeros(1, H, p + 1, d, dtype=torch.float64)
+        Q[0, :, p] = q[b]
+        ref, refL = sdpa_with_sink(Q, K[b:b + 1, :, :p + 1], V[b:b + 1, :, :p + 1],
+                                   torch_mask(p + 1, w, g).astype(bool), 0.25, sink)
+        assert np.allclose(Oh[b], ref[0, :, p].numpy(), atol=1e-12, rtol=0)
+        assert np.allclose(Lh[b], refL[0, :, p].numpy(), atol=1e-12, rtol=0)
+    # the rolling cache gives the same as the unbounded history
+    Kc = np.zeros((B, Hkv, w + g, d))
+    Vc = np.zeros((B, Hkv, w + g, d))
+    for b in range(B):
+        for p in range(int(pos[b]) + 1):
+            for kvh in range(Hkv):
+                place(Kc, Vc, oracle_mod, b, kvh, p, K[b, kvh, p].numpy(), V[b, kvh, p].numpy(), w, g)
+    Oc, Lc = oracle_mod.decode_cache(q, Kc, Vc, pos, w, g, 0.25, sink_logit=sink)
+    assert np.allclose(Oc, Oh, atol=1e-12, rtol=0)
+    assert np.allclose(Lc, Lh, atol=1e-12, rtol=0)
