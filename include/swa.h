@@ -88,6 +88,22 @@ int swa_prefill_ex(const void *Q, const void *K, const void *V, void *O, float *
                    int B, int H, int Hkv, int n, int d, int w, int g, float scale,
                    swa_dtype dtype, swa_stream_t stream);
 
+/*
+ * swa_prefill_sink_logit -- swa_prefill_ex with a learned per-head attention
+ * sink logit ("Sliding Window and Sparse Attention, from Longformer to CSA2",
+ * section 6, stage 3: a per-head logit that absorbs probability mass when no
+ * key is relevant).  For query head h the softmax gets one more entry, score
+ * sink_logit[h] (natural-log units, the same as scale * q.k) with a zero value
+ * vector:
+ *     O[i] = sum_j e^{s_ij} v_j / (e^{sink_logit[h]} + sum_j e^{s_ij}),
+ *     lse[i] = log(e^{sink_logit[h]} + sum_j e^{s_ij}).
+ * sink_logit: device fp32 [H] (4-byte aligned) or NULL (then this is
+ * swa_prefill_ex).  The token sinks of g are unaffected: both may be used.
+ */
+int swa_prefill_sink_logit(const void *Q, const void *K, const void *V, void *O, float *lse,
+                           const float *sink_logit, int B, int H, int Hkv, int n, int d, int w,
+                           int g, float scale, swa_dtype dtype, swa_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Decode: one query token per sequence against the rolling cache.         */
 /* ---------------------------------------------------------------------- */
@@ -129,6 +145,17 @@ int swa_decode_ex(const void *q, const void *Kcache, const void *Vcache, const i
                   int B, int H, int Hkv, int d, int w, int g, float scale, void *O,
                   float *lse, swa_dtype dtype, int num_splits, void *workspace,
                   size_t workspace_bytes, swa_stream_t stream);
+
+/*
+ * swa_decode_sink_logit -- swa_decode_ex with the learned per-head sink
+ * logit of swa_prefill_sink_logit (device fp32 [H] or NULL), applied in the
+ * log-sum-exp merge of the split results.
+ */
+int swa_decode_sink_logit(const void *q, const void *Kcache, const void *Vcache,
+                          const int32_t *pos, const float *sink_logit, int B, int H, int Hkv,
+                          int d, int w, int g, float scale, void *O, float *lse, swa_dtype dtype,
+                          int num_splits, void *workspace, size_t workspace_bytes,
+                          swa_stream_t stream);
 
 /*
  * swa_cache_append -- rolling-buffer scatter ("Sliding Window and Sparse

@@ -38,9 +38,12 @@ _i, _i64, _f, _p, _sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_v
 SIGNATURES = {
     "swa_prefill": (_i, [_p, _p, _p, _p] + [_i] * 7 + [_f, _p]),
     "swa_prefill_ex": (_i, [_p, _p, _p, _p, _p] + [_i] * 7 + [_f, _i, _p]),
+    "swa_prefill_sink_logit": (_i, [_p, _p, _p, _p, _p, _p] + [_i] * 7 + [_f, _i, _p]),
     "swa_decode": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p]),
     "swa_decode_workspace_bytes": (_sz, [_i] * 7),
     "swa_decode_ex": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p, _i, _i, _p, _sz, _p]),
+    "swa_decode_sink_logit": (_i, [_p, _p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p, _i, _i, _p, _sz,
+                                                                    _p]),
     "swa_decode_noalloc": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p]),
     "swa_cache_append": (_i, [_p, _p, _p, _p, _p] + [_i] * 6 + [_i, _p]),
     "swa_count_pairs": (_i64, [_i64, _i64, _i64]),
@@ -116,9 +119,11 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
 
 
 def prefill(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None, lse=None,
-            stream=None):
+            stream=None, sink_logit=None):
     """q [B,H,n,d], k/v [B,Hkv,n,d] (bf16 or fp32, CUDA) -> out [B,H,n,d].
-    lse: optional fp32 [B,H,n] output (natural-log log-sum-exp per row)."""
+    lse: optional fp32 [B,H,n] output (natural-log log-sum-exp per row).
+    sink_logit: optional fp32 [H] CUDA tensor of learned per-head sink logits
+    (swa_prefill_sink_logit)."""
     _need(q, "q")
     B, H, n, d = q.shape
     Hkv = k.shape[1]
@@ -132,6 +137,13 @@ def prefill(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None, l
     if lse is not None:
         _need(lse, "lse", torch.float32, (B, H, n))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if sink_logit is not None:
+        _need(sink_logit, "sink_logit", torch.float32, (H,))
+        rc = _load().swa_prefill_sink_logit(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                            _ptr(sink_logit), B, H, Hkv, n, d, int(w), int(g),
+                                            scale, _DT[q.dtype], _stream(stream, q.device))
+        _check("swa_prefill_sink_logit", rc)
+        return out
     rc = _load().swa_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, n, d,
                             int(w), int(g), scale, _DT[q.dtype], _stream(stream, q.device))
     _check("swa_prefill_ex", rc)
@@ -143,7 +155,7 @@ def decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits=0) -> int:
 
 
 def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = None, out=None,
-           lse=None, num_splits: int = 0, workspace=None, stream=None):
+           lse=None, num_splits: int = 0, workspace=None, stream=None, sink_logit=None):
     """q [B,H,d]; k_cache/v_cache [B,Hkv,w+g,d]; pos int32 [B] (CUDA) -> out [B,H,d].
     With workspace=None and lse=None and bf16 inputs this is swa_decode (library
     workspace); otherwise swa_decode_ex with a workspace allocated here if needed."""
@@ -158,7 +170,8 @@ def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = N
     _need(out, "out", q.dtype, q.shape)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     st = _stream(stream, q.device)
-    if workspace is None and lse is None and num_splits == 0 and q.dtype == torch.bfloat16:
+    if (workspace is None and lse is None and num_splits == 0 and q.dtype == torch.bfloat16
+            and sink_logit is None):
         rc = _load().swa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Hkv, d,
                             int(w), int(g), scale, _ptr(out), st)
         _check("swa_decode", rc)
@@ -169,6 +182,14 @@ def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = N
     if workspace is None and nbytes > 0:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if sink_logit is not None:
+        _need(sink_logit, "sink_logit", torch.float32, (H,))
+        rc = _load().swa_decode_sink_logit(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos),
+                                           _ptr(sink_logit), B, H, Hkv, d, int(w), int(g), scale,
+                                           _ptr(out), _ptr(lse), _DT[q.dtype], int(num_splits),
+                                           _ptr(workspace), ws_bytes, st)
+        _check("swa_decode_sink_logit", rc)
+        return out
     rc = _load().swa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Hkv, d,
                            int(w), int(g), scale, _ptr(out), _ptr(lse), _DT[q.dtype],
                            int(num_splits), _ptr(workspace), ws_bytes, st)

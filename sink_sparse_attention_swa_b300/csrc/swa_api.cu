@@ -38,22 +38,32 @@ Workspace g_ws[64];
 
 extern "C" {
 
-int swa_prefill_ex(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,
-                   int Hkv, int n, int d, int w, int g, float scale, swa_dtype dtype,
-                   swa_stream_t stream)
+int swa_prefill_sink_logit(const void *Q, const void *K, const void *V, void *O, float *lse,
+                           const float *sink_logit, int B, int H, int Hkv, int n, int d, int w,
+                           int g, float scale, swa_dtype dtype, swa_stream_t stream)
 {
     int rc = check_heads(B, H, Hkv, d, w, g);
     if (rc != SWA_OK) return rc;
     if (n < 1 || n > INT32_MAX - 256 || !scale_ok(scale)) return SWA_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SWA_ERR_INVALID_ARG;
     if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
+    if (sink_logit != nullptr && (reinterpret_cast<uintptr_t>(sink_logit) & 3u))
+        return SWA_ERR_INVALID_ARG;
     if (static_cast<long long>(B) * H * ((n + 127) / 128) > INT32_MAX) return SWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == SWA_BF16)
-        return launch_prefill_bf16(Q, K, V, O, lse, B, H, Hkv, n, d, w, g, scale, st);
+        return launch_prefill_bf16(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, d, w, g, scale, st);
     if (dtype == SWA_F32)
-        return launch_prefill_f32(Q, K, V, O, lse, B, H, Hkv, n, d, w, g, scale, st);
+        return launch_prefill_f32(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, d, w, g, scale, st);
     return SWA_ERR_INVALID_ARG;
+}
+
+int swa_prefill_ex(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,
+                   int Hkv, int n, int d, int w, int g, float scale, swa_dtype dtype,
+                   swa_stream_t stream)
+{
+    return swa_prefill_sink_logit(Q, K, V, O, lse, nullptr, B, H, Hkv, n, d, w, g, scale, dtype,
+                                  stream);
 }
 
 int swa_prefill(const void *Q, const void *K, const void *V, void *O, int B, int H, int Hkv, int n,
@@ -68,10 +78,11 @@ size_t swa_decode_workspace_bytes(int B, int H, int Hkv, int d, int w, int g, in
     return decode_workspace_bytes(B, H, Hkv, d, decode_ctas(B, Hkv, w, g, num_splits));
 }
 
-int swa_decode_ex(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos, int B,
-                  int H, int Hkv, int d, int w, int g, float scale, void *O, float *lse,
-                  swa_dtype dtype, int num_splits, void *workspace, size_t workspace_bytes,
-                  swa_stream_t stream)
+int swa_decode_sink_logit(const void *q, const void *Kcache, const void *Vcache,
+                          const int32_t *pos, const float *sink_logit, int B, int H, int Hkv,
+                          int d, int w, int g, float scale, void *O, float *lse, swa_dtype dtype,
+                          int num_splits, void *workspace, size_t workspace_bytes,
+                          swa_stream_t stream)
 {
     int rc = check_heads(B, H, Hkv, d, w, g);
     if (rc != SWA_OK) return rc;
@@ -83,12 +94,23 @@ int swa_decode_ex(const void *q, const void *Kcache, const void *Vcache, const i
         pos == nullptr || (reinterpret_cast<uintptr_t>(pos) & 3u))
         return SWA_ERR_INVALID_ARG;
     if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
+    if (sink_logit != nullptr && (reinterpret_cast<uintptr_t>(sink_logit) & 3u))
+        return SWA_ERR_INVALID_ARG;
     const int ctas = decode_ctas(B, Hkv, w, g, num_splits);
     const size_t need = decode_workspace_bytes(B, H, Hkv, d, ctas);
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
         return SWA_ERR_WORKSPACE;
-    return launch_decode(q, Kcache, Vcache, pos, B, H, Hkv, d, w, g, scale, O, lse, dtype, ctas,
-                         workspace, reinterpret_cast<cudaStream_t>(stream));
+    return launch_decode(q, Kcache, Vcache, pos, sink_logit, B, H, Hkv, d, w, g, scale, O, lse,
+                         dtype, ctas, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int swa_decode_ex(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos, int B,
+                  int H, int Hkv, int d, int w, int g, float scale, void *O, float *lse,
+                  swa_dtype dtype, int num_splits, void *workspace, size_t workspace_bytes,
+                  swa_stream_t stream)
+{
+    return swa_decode_sink_logit(q, Kcache, Vcache, pos, nullptr, B, H, Hkv, d, w, g, scale, O, lse,
+                                 dtype, num_splits, workspace, workspace_bytes, stream);
 }
 
 int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos, int B,

@@ -158,6 +158,7 @@ struct DecodeParams {
     float *ws;      // partials [P + B*Hkv][G][HD + 2]: m, l, o
     void *O;        // [B][H][d]
     float *lse;     // [B][H] or null
+    const float *sink;  // per-head sink logits [H] or null
 };
 
 __host__ __device__ __forceinline__ long long cta_begin(long long T, int P, int c)
@@ -575,8 +576,11 @@ __global__ void __launch_bounds__(G * HD) swa_decode_merge(const DecodeParams p)
     }
     const int b = bk / p.Hkv, h = (bk % p.Hkv) * G + hh;
     const size_t bh = static_cast<size_t>(b) * p.H + h;
-    static_cast<T *>(p.O)[bh * HD + col] = U::from_f(L > 0.f ? o / L : 0.f);
-    if (col == 0 && p.lse != nullptr) p.lse[bh] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+    float row_lse;
+    const float f = L > 0.f ? finish_row(M, L, p.sink, h, &row_lse) : 0.f;
+    if (!(L > 0.f)) row_lse = -INFINITY;
+    static_cast<T *>(p.O)[bh * HD + col] = U::from_f(o * f);
+    if (col == 0 && p.lse != nullptr) p.lse[bh] = row_lse;
 }
 
 template <typename T, int HD, int G>
@@ -703,7 +707,8 @@ size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int ctas)
            (static_cast<size_t>(d) + 2) * sizeof(float);
 }
 
-int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *pos, int B, int H,
+int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *pos,
+                  const float *sink, int B, int H,
                   int Hkv, int d, int w, int g, float scale, void *O, float *lse, swa_dtype dt,
                   int ctas, void *ws, cudaStream_t stream)
 {
@@ -722,6 +727,7 @@ int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *
     p.ws = static_cast<float *>(ws);
     p.O = O;
     p.lse = lse;
+    p.sink = sink;
     const int G = H / Hkv;
     if (dt == SWA_BF16) {
         if (d == 128) return dispatch_g<__nv_bfloat16, 128>(q, Kc, Vc, p, G, stream);

@@ -2,6 +2,7 @@
 // Not part of the public ABI (that is include/swa.h).
 #pragma once
 
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 
@@ -68,6 +69,32 @@ __host__ __device__ inline bool tile_full(const TileRange &r, int kt, int w, int
 }
 
 // ---------------------------------------------------------------------------
+// Final normalisation of a row's online softmax kept in base 2: m is the
+// reference maximum (scores times scale*log2(e)) and l the sum of
+// exp2(score - m).  An optional learned sink logit of the row's head
+// ("Sliding Window and Sparse Attention, from Longformer to CSA2", section 6,
+// stage 3: a per-head logit that absorbs mass, i.e. one more softmax entry
+// with a zero value) joins the normalising sum: sink [H] in natural-log
+// units, or null.  Returns the factor the unnormalised output is multiplied
+// by and sets *lse (natural log).  Without a sink this is 1/l and m + log2 l.
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+__device__ __forceinline__ float finish_row(float m, float l, const float *sink, int h, float *lse)
+{
+    const float sig = (sink != nullptr) ? sink[h] * 1.4426950408889634f : -INFINITY;
+    const float M = fmaxf(m, sig);
+    if (M == -INFINITY) {
+        *lse = -INFINITY;
+        return 0.f;
+    }
+    const float a = exp2f(m - M);
+    const float L = l * a + exp2f(sig - M);
+    *lse = (M + log2f(L)) * 0.69314718055994530942f;
+    return L > 0.f ? a / L : 0.f;
+}
+#endif
+
+// ---------------------------------------------------------------------------
 // Device status word (one per device, in swa_status.cu).  Kernels OR an error
 // code into it when a bounded wait runs out.
 // ---------------------------------------------------------------------------
@@ -79,17 +106,19 @@ int read_and_clear_status(cudaStream_t stream);
 // ---------------------------------------------------------------------------
 // Launchers (each validates nothing: the public entry points do that).
 // ---------------------------------------------------------------------------
+// sink: per-head sink logits [H] (device, fp32) or null, for every launcher.
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
-                        int B, int H, int Hkv, int n, int d, int w, int g, float scale,
-                        cudaStream_t stream);
+                        const float *sink, int B, int H, int Hkv, int n, int d, int w, int g,
+                        float scale, cudaStream_t stream);
 int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
-                       int B, int H, int Hkv, int n, int d, int w, int g, float scale,
-                       cudaStream_t stream);
+                       const float *sink, int B, int H, int Hkv, int n, int d, int w, int g,
+                       float scale, cudaStream_t stream);
 // CTAs of the decode split pass: num_splits > 0 asks for about that many per
 // (sequence, kv head); 0 picks one resident wave on the current device.
 int decode_ctas(int B, int Hkv, int w, int g, int num_splits);
 size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int ctas);
-int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *pos, int B,
+int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *pos,
+                  const float *sink, int B,
                   int H, int Hkv, int d, int w, int g, float scale, void *O, float *lse,
                   swa_dtype dt, int ctas, void *ws, cudaStream_t stream);
 int launch_cache_append(void *Kc, void *Vc, const void *kn, const void *vn, const int32_t *pos0,

@@ -22,7 +22,8 @@ template <int HD>
 __global__ void __launch_bounds__(TM)
     swa_prefill_f32_simt(const float *__restrict__ Q, const float *__restrict__ K,
                          const float *__restrict__ V, float *__restrict__ O,
-                         float *__restrict__ lse, int H, int Hkv, int n, int w, int g, float sl2)
+                         float *__restrict__ lse, const float *__restrict__ sink, int H,
+                         int Hkv, int n, int w, int g, float sl2)
 {
     __shared__ __align__(16) float sK[TN][HD];
     __shared__ __align__(16) float sV[TN][HD];
@@ -86,33 +87,34 @@ __global__ void __launch_bounds__(TM)
         m = m_new;
     }
     if (i < n) {
-        const float inv = 1.f / l;
+        float row_lse;
+        const float inv = finish_row(m, l, sink, h, &row_lse);
 #pragma unroll
         for (int e = 0; e < HD; ++e) O[qrow * HD + e] = acc[e] * inv;
-        if (lse != nullptr) lse[qrow] = (m + log2f(l)) * 0.69314718055994530942f;
+        if (lse != nullptr) lse[qrow] = row_lse;
     }
 }
 
 template <int HD>
-int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,
-              int Hkv, int n, int w, int g, float scale, cudaStream_t stream)
+int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, const float *sink,
+              int B, int H, int Hkv, int n, int w, int g, float scale, cudaStream_t stream)
 {
     dim3 grid((n + TM - 1) / TM, H, B);
     swa_prefill_f32_simt<HD><<<grid, TM, 0, stream>>>(
         static_cast<const float *>(Q), static_cast<const float *>(K),
-        static_cast<const float *>(V), static_cast<float *>(O), lse, H, Hkv, n, w, g,
+        static_cast<const float *>(V), static_cast<float *>(O), lse, sink, H, Hkv, n, w, g,
         scale * 1.4426950408889634f);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
-                       int H, int Hkv, int n, int d, int w, int g, float scale,
-                       cudaStream_t stream)
+int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
+                       const float *sink, int B, int H, int Hkv, int n, int d, int w, int g,
+                       float scale, cudaStream_t stream)
 {
-    if (d == 64) return launch_hd<64>(Q, K, V, O, lse, B, H, Hkv, n, w, g, scale, stream);
-    if (d == 128) return launch_hd<128>(Q, K, V, O, lse, B, H, Hkv, n, w, g, scale, stream);
+    if (d == 64) return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, w, g, scale, stream);
+    if (d == 128) return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, w, g, scale, stream);
     return SWA_ERR_UNSUPPORTED;
 }
 

@@ -88,6 +88,7 @@ struct PrefillParams {
     float sl2;  // scale * log2(e)
     __nv_bfloat16 *O;
     float *lse;
+    const float *sink;  // per-head sink logits [H] or null
     int *status;
 };
 
@@ -447,7 +448,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             }
             tc_fence_after();
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            float row_lse;
+            const float inv_l = finish_row(m, l, p.sink, h, &row_lse);
             __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + i) * HD;
 #pragma unroll 1
             for (int q = 0; q < HD / 32; ++q) {
@@ -471,8 +473,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY));
             if (p.lse != nullptr && i < p.n)
-                p.lse[static_cast<size_t>(b * p.H + h) * p.n + i] =
-                    (m + log2f(l)) * 0.69314718055994530942f;
+                p.lse[static_cast<size_t>(b * p.H + h) * p.n + i] = row_lse;
         }
     }
 #undef BAR
@@ -916,7 +917,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 break;
             }
             tc_fence_after();
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            float row_lse;
+            const float inv_l = finish_row(m, l, p.sink, h, &row_lse);
             __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + i) * HD;
 #pragma unroll 1
             for (int q = 0; q < HD / 32; ++q) {
@@ -940,8 +942,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY + x));
             if (p.lse != nullptr && i < p.n)
-                p.lse[static_cast<size_t>(b * p.H + h) * p.n + i] =
-                    (m + log2f(l)) * 0.69314718055994530942f;
+                p.lse[static_cast<size_t>(b * p.H + h) * p.n + i] = row_lse;
         }
     }
 #undef BAR
@@ -1088,8 +1089,8 @@ bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
 }
 
 template <int HD>
-int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,
-              int Hkv, int n, int w, int g, float scale, cudaStream_t stream)
+int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, const float *sink,
+              int B, int H, int Hkv, int n, int w, int g, float scale, cudaStream_t stream)
 {
     using L = Layout<HD>;
     CUtensorMap mq, mk, mv;
@@ -1117,6 +1118,7 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     p.sl2 = scale * 1.4426950408889634f;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.lse = lse;
+    p.sink = sink;
     p.status = status_ptr();
     if (p.status == nullptr) return SWA_ERR_CUDA;
     if (p.G % 2 == 0 && std::getenv("SWA_PREFILL_SINGLE") == nullptr) {
@@ -1142,12 +1144,12 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
 
 }  // namespace
 
-int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
-                        int H, int Hkv, int n, int d, int w, int g, float scale,
-                        cudaStream_t stream)
+int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
+                        const float *sink, int B, int H, int Hkv, int n, int d, int w, int g,
+                        float scale, cudaStream_t stream)
 {
-    if (d == 128) return launch_hd<128>(Q, K, V, O, lse, B, H, Hkv, n, w, g, scale, stream);
-    if (d == 64) return launch_hd<64>(Q, K, V, O, lse, B, H, Hkv, n, w, g, scale, stream);
+    if (d == 128) return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, w, g, scale, stream);
+    if (d == 64) return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, w, g, scale, stream);
     return SWA_ERR_UNSUPPORTED;
 }
 
