@@ -42,6 +42,9 @@ PREFILL_WORKLOADS = {
     "mistral_like_prefill": dict(B=1, H=32, Hkv=8, n=16384, d=128, w=4096, g=0, sink_scale=1.0),
     "gemma3_local_prefill": dict(B=2, H=32, Hkv=16, n=32768, d=128, w=1024, g=0, sink_scale=1.0),
     "long_sink_prefill": dict(B=1, H=32, Hkv=8, n=131072, d=128, w=4096, g=4, sink_scale=4.0),
+    # the full-causal global layer of the Gemma-3 hybrid (w >= n)
+    "gemma3_global_prefill": dict(B=2, H=32, Hkv=16, n=32768, d=128, w=32768, g=0,
+                                  sink_scale=1.0),
 }
 PREFILL = PREFILL_WORKLOADS["mistral_like_prefill"]
 DECODE = dict(B=32, H=32, Hkv=8, d=128, w=4096, g=4, pos=100000, sink_scale=4.0)

@@ -13,6 +13,8 @@ Workloads (the shapes come from the model families the pages quote):
   gemma3_local_prefill    B=2 H=32 Hkv=16 n=32768 d=128 w=1024 g=0, bf16
   long_sink_prefill       B=1 H=32 Hkv=8 n=131072 d=128 w=4096 g=4, bf16,
                           sink keys (positions 0..3) scaled x4
+  gemma3_global_prefill   B=2 H=32 Hkv=16 n=32768 d=128 w=n (full causal) g=0,
+                          bf16: the global layer between the local ones
 """
 from __future__ import annotations
 
@@ -32,6 +34,8 @@ WORKLOADS = {
                                  g=0, dtype="bf16", sink_scale=1.0),
     "long_sink_prefill": dict(kind="prefill", B=1, H=32, Hkv=8, n=131072, d=128, w=4096,
                               g=4, dtype="bf16", sink_scale=4.0),
+    "gemma3_global_prefill": dict(kind="prefill", B=2, H=32, Hkv=16, n=32768, d=128, w=32768,
+                                  g=0, dtype="bf16", sink_scale=1.0),
 }
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
