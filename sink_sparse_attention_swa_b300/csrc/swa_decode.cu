@@ -564,11 +564,32 @@ __global__ void __launch_bounds__(G * HD) swa_decode_merge(const DecodeParams p)
     const int hh = threadIdx.x / HD, col = threadIdx.x % HD;
     const long long S = static_cast<long long>(p.w) + p.g;
     const int c_lo = cta_of(p.T, p.P, bk * S), c_hi = cta_of(p.T, p.P, bk * S + S - 1);
-    float M = M_EMPTY;
-    for (int c = c_lo; c <= c_hi; ++c)
+    // the first NU partials (usually all of them) are loaded in one round
+    constexpr int NU = 4;
+    float mv[NU], lv[NU], ov[NU];
+#pragma unroll
+    for (int k = 0; k < NU; ++k) {
+        mv[k] = M_EMPTY;
+        lv[k] = 0.f;
+        ov[k] = 0.f;
+        if (c_lo + k <= c_hi) {
+            const float *x = p.ws + ((static_cast<size_t>(c_lo + k) + bk) * G + hh) * (HD + 2);
+            mv[k] = x[0];
+            lv[k] = x[1];
+            ov[k] = x[2 + col];
+        }
+    }
+    float M = fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3]));
+    for (int c = c_lo + NU; c <= c_hi; ++c)
         M = fmaxf(M, p.ws[((static_cast<size_t>(c) + bk) * G + hh) * (HD + 2)]);
     float L = 0.f, o = 0.f;
-    for (int c = c_lo; c <= c_hi; ++c) {
+#pragma unroll
+    for (int k = 0; k < NU; ++k) {
+        const float sc = ex2(mv[k] - M);
+        L += sc * lv[k];
+        o += sc * ov[k];
+    }
+    for (int c = c_lo + NU; c <= c_hi; ++c) {
         const float *x = p.ws + ((static_cast<size_t>(c) + bk) * G + hh) * (HD + 2);
         const float sc = ex2(x[0] - M);
         L += sc * x[1];

@@ -502,6 +502,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // that O_X may be rescaled.
 // ------------------------------------------------------------------------
 constexpr int NTHREADS2 = 384;
+// named barriers 1 (head A) and 2 (head B): a softmax warpgroup's 128 threads
+// arrive when P is in tensor memory, the 32 threads of the MMA warp wait
+constexpr int P_BAR_THREADS = 128 + 32;
 // registers per thread after the hand-over: 128 * (56 + 224 + 224) equals the
 // 384 * 168 registers the kernel is launched with
 constexpr int REGS_CTRL = 88;
@@ -558,6 +561,15 @@ __device__ __forceinline__ void decode_pair_item(int r, const PrefillParams &p, 
     kvh = r % p.Hkv;
     b = r / p.Hkv;
     h0 = kvh * p.G + 2 * hp;
+}
+
+// Softmax warpgroup x: P_x of the current key tile is in tensor memory.
+__device__ __forceinline__ void p_arrive(int x)
+{
+    if (x == 0)
+        asm volatile("bar.arrive 1, %0;" ::"n"(128 + 32) : "memory");
+    else
+        asm volatile("bar.arrive 2, %0;" ::"n"(128 + 32) : "memory");
 }
 
 __device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi)
@@ -734,8 +746,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             // P_X(prev) V into O_X
             auto issue_pv = [&](auto xc) -> bool {
                 constexpr int x = decltype(xc)::value;
-                if (!warp_wait(BAR(L::P_FULL + x), prev_c & 1, abort_flag, p.status))
-                    return false;
+                // P_X(prev) stored: softmax warpgroup X arrives on named barrier
+                // 1 + x (a hardware barrier wakes the issuer sooner than an
+                // mbarrier).  A warpgroup that gives up arrives once more and sets
+                // the abort flag, which is checked after every meeting, so this
+                // never waits for an arrival that will not come.
+                asm volatile("bar.sync %0, %1;" ::"n"(1 + x), "n"(P_BAR_THREADS) : "memory");
+                if (*abort_flag) return false;
                 if (prev_first && !warp_wait(BAR(L::O_EMPTY + x), (prev_it & 1) ^ 1, abort_flag,
                                              p.status))
                     return false;
@@ -908,7 +925,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(L::P_FULL + x));
+                p_arrive(x);
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
@@ -943,6 +960,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY + x));
             if (p.lse != nullptr && i < p.n)
                 p.lse[static_cast<size_t>(b * p.H + h) * p.n + i] = row_lse;
+        }
+        // gave up (a wait ran out): one more arrival lets an issuer that is
+        // already waiting for this head's P meet, see the abort flag and stop
+        if (!ok) {
+            *abort_flag = 1;
+            __syncwarp();
+            p_arrive(x);
         }
     }
 #undef BAR
