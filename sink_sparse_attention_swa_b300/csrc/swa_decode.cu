@@ -21,10 +21,10 @@
 // all (sequence, kv head) segments, laid end to end (B*Hkv*(w+g) rows), are
 // cut into P equal contiguous ranges, one per CTA, so every CTA streams the
 // same number of bytes whatever B, Hkv and w are.  In each CTA one producer
-// thread copies the valid rows of its range, 32 at a time, into a ring of
+// thread copies the valid rows of its range, 64 at a time, into a ring of
 // shared-memory stages with bulk asynchronous copies (cp.async.bulk, one per
 // contiguous run of rows, completion on an mbarrier); four consumer warps take
-// 8 rows of each stage each.  A consumer warp
+// two groups of 8 rows of each stage each.  A consumer warp
 //   * scores its 8 keys against the G query heads of the group with packed
 //     fp32x2 FMAs (8 lanes per key row, q pre-scaled by scale*log2(e)),
 //   * finishes the dot products with a reduce-scatter butterfly over the 8
@@ -53,13 +53,14 @@ using namespace ptx;
 
 constexpr int DEC_CWARPS = 4;                       // consumer warps per CTA
 constexpr int DEC_THREADS = (DEC_CWARPS + 1) * 32;  // + one producer warp
-constexpr int GROUP_ROWS = 8;                       // rows a consumer warp takes per stage
-constexpr int STAGE_ROWS = DEC_CWARPS * GROUP_ROWS;
+constexpr int GROUP_ROWS = 8;                       // rows of one consumer-warp group
+constexpr int DEC_GPW = 2;                          // groups per consumer warp per stage
+constexpr int STAGE_ROWS = DEC_CWARPS * GROUP_ROWS * DEC_GPW;
 constexpr int DEC_CTAS_PER_SM = 2;
+constexpr int DEC_STAGE_BUDGET = 96 * 1024;         // shared memory for the stage ring
 constexpr int MIN_SLOTS_PER_CTA = 64;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr float M_EMPTY = -1.0e30f;  // running max before any key (finite: no inf-inf)
-constexpr float LN2 = 0.69314718055994530942f;
 constexpr uint64_t DEC_TIMEOUT_NS = 2000000000ull;
 
 __device__ __forceinline__ float ex2(float x)
@@ -133,7 +134,7 @@ struct DecCfg {
     static constexpr int EV = HD / 16;    // columns per lane
     static constexpr int VB = EV * static_cast<int>(sizeof(T));  // bytes per lane per value row
     static constexpr int STAGE_BYTES = 2 * STAGE_ROWS * RB;
-    static constexpr int NS_RAW = (96 * 1024) / STAGE_BYTES;
+    static constexpr int NS_RAW = (DEC_STAGE_BUDGET) / STAGE_BYTES;
     static constexpr int NS = NS_RAW < 2 ? 2 : (NS_RAW > 8 ? 8 : NS_RAW);  // stages
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = NS * STAGE_ROWS * RB;
@@ -365,7 +366,9 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
         if (!__all_sync(0xffffffffu,
                         mbar_wait(FULL(slot), ph, abort_flag, p.status, DEC_TIMEOUT_NS)))
             return false;
-        const int row0 = warp * GROUP_ROWS;
+#pragma unroll 1
+        for (int gi = 0; gi < DEC_GPW; ++gi) {
+        const int row0 = (gi * DEC_CWARPS + warp) * GROUP_ROWS;
         const int nrows = count - row0;  // rows of this warp's group that exist (may be <= 0)
         if (nrows > 0) {
             const uint8_t *kst = smem + C::K_OFF + (slot * STAGE_ROWS + row0) * C::RB;
@@ -483,7 +486,8 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
                 }
             }
         }
-        __syncwarp();
+        __syncwarp();  // the warp's P rows are reused by its next group
+        }
         if (lane == 0) mbar_arrive(EMPTY(slot));
         return true;
     };
