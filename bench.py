@@ -47,6 +47,8 @@ PREFILL_WORKLOADS = {
                                   sink_scale=1.0),
 }
 PREFILL = PREFILL_WORKLOADS["mistral_like_prefill"]
+# a prompt chunk of T tokens at position pos0 against a full rolling cache
+CHUNK = dict(B=4, H=32, Hkv=8, d=128, w=4096, g=4, T=4096, pos0=100000, sink_scale=4.0)
 DECODE = dict(B=32, H=32, Hkv=8, d=128, w=4096, g=4, pos=100000, sink_scale=4.0)
 METRIC = "SWA prefill useful TFLOP/s (% bf16 peak); decode HBM GB/s (% peak)"
 PREFILL_KERNEL_SRC = os.path.join(ROOT, "sink_sparse_attention_swa_b300", "csrc", "swa_prefill_tc.cu")
@@ -65,6 +67,15 @@ def pairs(n, w, g):
 
 def prefill_flops(c):
     return 4 * pairs(c["n"], c["w"], c["g"]) * c["d"] * c["B"] * c["H"]
+
+
+def chunk_flops(c):
+    """Useful FLOPs of a chunk: query position P reads min(P+1, w) window keys
+    plus min(g, P+1-w) sinks once the window has moved past them."""
+    keys = 0
+    for P in range(c["pos0"], c["pos0"] + c["T"]):
+        keys += min(P + 1, c["w"]) + (min(c["g"], P + 1 - c["w"]) if P + 1 > c["w"] else 0)
+    return 4 * keys * c["d"] * c["B"] * c["H"]
 
 
 def decode_bytes(c, elem=2):
@@ -366,6 +377,92 @@ def run_swa(args):
     print(json.dumps(line), flush=True)
 
 
+def run_chunk(args):
+    """Chunked prefill into the rolling cache, the serving call: one
+    swa_prefill_chunk with append (gather the key lists, append the chunk to
+    the cache, tensor-core attention) per step."""
+    import sink_sparse_attention_swa_b300 as swa
+    from sink_sparse_attention_swa_b300 import synthetic
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    pk = peaks()
+    c = CHUNK
+    flush = L2Flush(dev)
+    flops = chunk_flops(c)
+    x = synthetic.chunk_inputs(c["B"], c["H"], c["Hkv"], c["d"], c["w"], c["g"], c["T"],
+                               c["pos0"], seed=rank, sink_scale=c["sink_scale"], device=dev)
+    out = torch.empty_like(x.q)
+    nbytes = swa.prefill_chunk_workspace_bytes(c["B"], c["Hkv"], c["T"], c["d"], c["w"], c["g"])
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    fn = lambda: swa.prefill_chunk(x.q, x.k_new, x.v_new, x.Kc, x.Vc, x.pos0, c["w"], c["g"],
+                                   x.scale, out=out, append=True, workspace=ws, stream=stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        times = time_launches(fn, args.steps, args.warmup, flush, stream)
+    barrier(world)
+    ms = max_over_ranks(float(np.mean(times)), world, dev)
+    launch_ms = float(np.mean(times))
+    e2e = None
+    if not args.no_e2e:
+        qh = x.q.cpu().pin_memory()
+        kh = x.k_new.cpu().pin_memory()
+        vh = x.v_new.cpu().pin_memory()
+        oh = torch.empty_like(qh).pin_memory()
+        qd, kd, vd = torch.empty_like(x.q), torch.empty_like(x.k_new), torch.empty_like(x.v_new)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            swa.prefill_chunk(qd, kd, vd, x.Kc, x.Vc, x.pos0, c["w"], c["g"], x.scale, out=out,
+                              append=True, workspace=ws, stream=stream)
+            oh.copy_(out, non_blocking=True)
+
+        e2e_times = time_launches(e2e_step, max(2, args.steps // 2), 2, flush, stream)
+        e2e_ms = max_over_ranks(float(np.mean(e2e_times)), world, dev)
+        e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": (qh.numel() + kh.numel() + vh.numel()) * 2,
+               "d2h_bytes_per_step": oh.numel() * 2, "ms_per_step": e2e_ms,
+               "note": "chunk q/k/v from pinned host memory, O back; the cache stays on the GPU"}
+    assert swa.device_status(stream) == 0, "device status reported an error"
+    if rank != 0:
+        return
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": flops * world / (ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "chunked_prefill_stream", **c, "scale": "1/sqrt(d)",
+                   "step": "swa_prefill_chunk with append (gather + cache append + attention)",
+                   "l2": "flushed before each timed launch: 256 MiB write, then 256 MiB read (L2 left clean)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"],
+                     "unit": "TFLOP/s", "frac": achieved / pk["bf16"], "traffic": None,
+                     "kernel": "whole call: swa_chunk_gather_k + swa_cache_append_k + "
+                               "swa_prefill_bf16_pair_sm103",
+                     "peak_source": pk["src"] + " burst",
+                     "useful_flops_per_launch": flops},
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def decode_leg(args, swa, synthetic, world, rank, local, dev, stream, flush, pk):
     dc = DECODE
     dx = synthetic.decode_cache_inputs(dc["B"], dc["H"], dc["Hkv"], dc["d"], dc["w"], dc["g"],
@@ -457,13 +554,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"])
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "chunk"])
     ap.add_argument("--workload", default="mistral_like_prefill", choices=sorted(PREFILL_WORKLOADS))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only == "chunk":
+        run_chunk(args)
     else:
         run_swa(args)
     if torch.distributed.is_initialized():

@@ -104,6 +104,39 @@ int swa_prefill_sink_logit(const void *Q, const void *K, const void *V, void *O,
                            const float *sink_logit, int B, int H, int Hkv, int n, int d, int w,
                            int g, float scale, swa_dtype dtype, swa_stream_t stream);
 
+/*
+ * swa_prefill_chunk -- chunked prefill into the rolling cache: T new tokens
+ * of each sequence at positions pos0[b] .. pos0[b]+T-1 attend, with the
+ * window and sink rule above, to the keys the rolling cache holds for the
+ * positions before pos0[b] and to their own keys ("Sliding Window and Sparse
+ * Attention, from Longformer to CSA2", section 1: prefill reads many
+ * positions at once; section 2: the rolling buffer and the sinks).  This is
+ * the step that takes a long prompt into the cache piece by piece.
+ *   Q, O [B][H][T][d]; k_new, v_new [B][Hkv][T][d] (the chunk's keys and
+ *   values); Kcache, Vcache [B][Hkv][w+g][d] holding every position before
+ *   pos0[b] that the rolling cache keeps (appended with swa_cache_append);
+ *   pos0: device int32 [B], >= 0; lse [B][H][T] fp32 or NULL; sink_logit
+ *   [H] fp32 or NULL (as in swa_prefill_sink_logit).  dtype: SWA_BF16
+ *   (tensor cores) or SWA_F32.
+ * append = 0: the cache is only read (append the chunk afterwards with
+ * swa_cache_append).  append != 0: after the keys are laid out in the
+ * workspace, the chunk is written into Kcache/Vcache exactly as
+ * swa_cache_append would write it, in stream order, so one call leaves the
+ * cache holding positions up to pos0[b]+T-1 for the next chunk or decode step;
+ * the attention itself reads the workspace copy and so sees the cache as it
+ * was before the call.  workspace: caller-
+ * owned device memory of at least swa_prefill_chunk_workspace_bytes(...)
+ * bytes (16-byte aligned, no initialisation needed), where the kernel lays
+ * out each sequence's keys in position order before the tensor-core pass.
+ */
+size_t swa_prefill_chunk_workspace_bytes(int B, int Hkv, int T, int d, int w, int g,
+                                         swa_dtype dtype);
+int swa_prefill_chunk(const void *Q, const void *k_new, const void *v_new, void *Kcache,
+                      void *Vcache, const int32_t *pos0, void *O, float *lse,
+                      const float *sink_logit, int B, int H, int Hkv, int T, int d, int w, int g,
+                      float scale, int append, swa_dtype dtype, void *workspace,
+                      size_t workspace_bytes, swa_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Decode: one query token per sequence against the rolling cache.         */
 /* ---------------------------------------------------------------------- */

@@ -20,7 +20,7 @@ import os
 import torch
 
 __all__ = [
-    "SwaError", "prefill", "decode", "cache_append", "decode_workspace_bytes",
+    "SwaError", "prefill", "prefill_chunk", "decode", "cache_append", "decode_workspace_bytes",
     "count_pairs", "enumerate_tiles", "cache_slot", "device_status", "selftest_umma",
     "library_path", "lib",
 ]
@@ -39,6 +39,8 @@ SIGNATURES = {
     "swa_prefill": (_i, [_p, _p, _p, _p] + [_i] * 7 + [_f, _p]),
     "swa_prefill_ex": (_i, [_p, _p, _p, _p, _p] + [_i] * 7 + [_f, _i, _p]),
     "swa_prefill_sink_logit": (_i, [_p, _p, _p, _p, _p, _p] + [_i] * 7 + [_f, _i, _p]),
+    "swa_prefill_chunk_workspace_bytes": (_sz, [_i] * 7),
+    "swa_prefill_chunk": (_i, [_p] * 9 + [_i] * 7 + [_f, _i, _i, _p, _sz, _p]),
     "swa_decode": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p]),
     "swa_decode_workspace_bytes": (_sz, [_i] * 7),
     "swa_decode_ex": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p, _i, _i, _p, _sz, _p]),
@@ -148,6 +150,51 @@ def prefill(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None, l
                             int(w), int(g), scale, _DT[q.dtype], _stream(stream, q.device))
     _check("swa_prefill_ex", rc)
     return out
+
+
+def prefill_chunk(q, k_new, v_new, k_cache, v_cache, pos0, w: int, g: int = 0,
+                  scale: float | None = None, out=None, lse=None, sink_logit=None,
+                  append: bool = False, workspace=None, stream=None):
+    """Chunked prefill (swa_prefill_chunk): q [B,H,T,d] at positions
+    pos0[b] .. pos0[b]+T-1 (pos0 int32 [B], CUDA) against the rolling caches
+    [B,Hkv,w+g,d] and the chunk's own k_new/v_new [B,Hkv,T,d] -> out [B,H,T,d].
+    append=False only reads the caches; append=True also writes the chunk into
+    them (as cache_append does) in the same call."""
+    _need(q, "q")
+    B, H, T, d = q.shape
+    Hkv = k_new.shape[1]
+    _need(k_new, "k_new", q.dtype, (B, Hkv, T, d))
+    _need(v_new, "v_new", q.dtype, (B, Hkv, T, d))
+    _need(k_cache, "k_cache", q.dtype, (B, Hkv, w + g, d))
+    _need(v_cache, "v_cache", q.dtype, (B, Hkv, w + g, d))
+    _need(pos0, "pos0", torch.int32, (B,))
+    if q.dtype not in _DT:
+        raise TypeError("q must be bfloat16 or float32")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, T))
+    if sink_logit is not None:
+        _need(sink_logit, "sink_logit", torch.float32, (H,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = int(_load().swa_prefill_chunk_workspace_bytes(B, Hkv, T, d, int(w), int(g),
+                                                           _DT[q.dtype]))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = _load().swa_prefill_chunk(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                   _ptr(v_cache), _ptr(pos0), _ptr(out), _ptr(lse),
+                                   _ptr(sink_logit), B, H, Hkv, T, d, int(w), int(g), scale,
+                                   int(bool(append)), _DT[q.dtype], _ptr(workspace), ws_bytes,
+                                   _stream(stream, q.device))
+    _check("swa_prefill_chunk", rc)
+    return out
+
+
+def prefill_chunk_workspace_bytes(B, Hkv, T, d, w, g, dtype=torch.bfloat16) -> int:
+    return int(_load().swa_prefill_chunk_workspace_bytes(B, Hkv, T, d, int(w), int(g),
+                                                         _DT[dtype]))
 
 
 def decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits=0) -> int:

@@ -52,10 +52,62 @@ int swa_prefill_sink_logit(const void *Q, const void *K, const void *V, void *O,
     if (static_cast<long long>(B) * H * ((n + 127) / 128) > INT32_MAX) return SWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == SWA_BF16)
-        return launch_prefill_bf16(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, d, w, g, scale, st);
+        return launch_prefill_bf16(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, w, g, scale,
+                                   nullptr, st);
     if (dtype == SWA_F32)
-        return launch_prefill_f32(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, d, w, g, scale, st);
+        return launch_prefill_f32(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, w, g, scale,
+                                  nullptr, st);
     return SWA_ERR_INVALID_ARG;
+}
+
+size_t swa_prefill_chunk_workspace_bytes(int B, int Hkv, int T, int d, int w, int g,
+                                         swa_dtype dtype)
+{
+    if (check_heads(B, Hkv, Hkv, d, w, g) != SWA_OK || T < 1) return 0;
+    if (dtype != SWA_BF16 && dtype != SWA_F32) return 0;
+    const size_t elem = dtype == SWA_BF16 ? 2 : 4;
+    return 2 * static_cast<size_t>(B) * Hkv * static_cast<size_t>(chunk_rows_max(w, g, T)) * d *
+           elem;
+}
+
+int swa_prefill_chunk(const void *Q, const void *k_new, const void *v_new, void *Kcache,
+                      void *Vcache, const int32_t *pos0, void *O, float *lse,
+                      const float *sink_logit, int B, int H, int Hkv, int T, int d, int w, int g,
+                      float scale, int append, swa_dtype dtype, void *workspace,
+                      size_t workspace_bytes, swa_stream_t stream)
+{
+    int rc = check_heads(B, H, Hkv, d, w, g);
+    if (rc != SWA_OK) return rc;
+    if (T < 1 || T > INT32_MAX - 256 || !scale_ok(scale)) return SWA_ERR_INVALID_ARG;
+    if (dtype != SWA_BF16 && dtype != SWA_F32) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(Kcache) ||
+        !aligned16(Vcache) || !aligned16(O) || pos0 == nullptr ||
+        (reinterpret_cast<uintptr_t>(pos0) & 3u))
+        return SWA_ERR_INVALID_ARG;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
+    if (sink_logit != nullptr && (reinterpret_cast<uintptr_t>(sink_logit) & 3u))
+        return SWA_ERR_INVALID_ARG;
+    const long long rows = chunk_rows_max(w, g, T);
+    if (rows > INT32_MAX - 256) return SWA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H * ((T + 127) / 128) > INT32_MAX) return SWA_ERR_INVALID_ARG;
+    const size_t need = swa_prefill_chunk_workspace_bytes(B, Hkv, T, d, w, g, dtype);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+        return SWA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *Kx = static_cast<uint8_t *>(workspace);
+    uint8_t *Vx = Kx + need / 2;
+    rc = launch_chunk_gather(Kx, Vx, Kcache, Vcache, k_new, v_new, pos0, B, Hkv, T, d, w, g, dtype,
+                             st);
+    if (rc != SWA_OK) return rc;
+    if (append) {  // the key lists are already copied out, so the ring may be overwritten
+        rc = launch_cache_append(Kcache, Vcache, k_new, v_new, pos0, T, B, Hkv, d, w, g, dtype, st);
+        if (rc != SWA_OK) return rc;
+    }
+    if (dtype == SWA_BF16)
+        return launch_prefill_bf16(Q, Kx, Vx, O, lse, sink_logit, B, H, Hkv, T,
+                                   static_cast<int>(rows), d, w, g, scale, pos0, st);
+    return launch_prefill_f32(Q, Kx, Vx, O, lse, sink_logit, B, H, Hkv, T, static_cast<int>(rows),
+                              d, w, g, scale, pos0, st);
 }
 
 int swa_prefill_ex(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,

@@ -35,11 +35,13 @@ struct TileRange {
     int count;    // total key tiles visited
 };
 
-__host__ __device__ inline TileRange tile_range(int qt, int n, int w, int g, int BM, int BN)
+// The key tiles for query rows q0 .. q1 (indices into the key list; any
+// alignment).
+__host__ __device__ inline TileRange tile_range_at(int q0, int q1, int w, int g, int BN)
 {
     TileRange r;
-    r.q0 = qt * BM;
-    r.q1 = (r.q0 + BM < n ? r.q0 + BM : n) - 1;
+    r.q0 = q0;
+    r.q1 = q1;
     int lo = r.q0 - w + 1;
     if (lo < 0) lo = 0;
     r.kt_lo = lo / BN;
@@ -53,6 +55,48 @@ __host__ __device__ inline TileRange tile_range(int qt, int n, int w, int g, int
     r.ns = ns;
     r.count = ns + (kt_hi - r.kt_lo + 1);
     return r;
+}
+
+__host__ __device__ inline TileRange tile_range(int qt, int n, int w, int g, int BM, int BN)
+{
+    const int q0 = qt * BM;
+    return tile_range_at(q0, (q0 + BM < n ? q0 + BM : n) - 1, w, g, BN);
+}
+
+// ---------------------------------------------------------------------------
+// Chunked prefill ("Sliding Window and Sparse Attention, from Longformer to
+// CSA2", section 2: the rolling buffer; section 1: prefill vs decode).  A
+// chunk of T new tokens at positions pos0 .. pos0+T-1 attends to the rolling
+// cache and to itself.  Its keys are laid out as one list:
+//   indices 0 .. S-1        positions 0 .. S-1 (the sinks, S = min(g, pos0)),
+//   indices S ..            positions W0 .. pos0+T-1 (window part of the
+//                           cache, then the chunk), W0 = max(S, pos0-w+1).
+// Positions S .. W0-1 are left out: no query of the chunk reads them.  Index
+// differences equal position differences after the sinks, and the sinks are
+// the first g indices (or all positions, when pos0 < g), so the prefill mask
+// (j <= i, j >= i-w+1 or j < g) holds on list indices with query t at index
+// t + chunk_offset.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline int chunk_sinks(int pos0, int g) { return pos0 < g ? pos0 : g; }
+__host__ __device__ inline int chunk_w0(int pos0, int w, int g)
+{
+    const int s = chunk_sinks(pos0, g), a = pos0 - w + 1;
+    return s > a ? s : a;
+}
+__host__ __device__ inline int chunk_offset(int pos0, int w, int g)
+{
+    return pos0 + chunk_sinks(pos0, g) - chunk_w0(pos0, w, g);
+}
+// rows of the key list for a chunk of T tokens at pos0
+__host__ __device__ inline int chunk_keys(int pos0, int w, int g, int T)
+{
+    return chunk_offset(pos0, w, g) + T;
+}
+// the largest key list over all pos0, rounded up to whole 128-row tiles
+__host__ __device__ inline long long chunk_rows_max(int w, int g, int T)
+{
+    const long long m = static_cast<long long>(g) + (w - 1) + T;
+    return (m + 127) / 128 * 128;
 }
 
 __host__ __device__ inline int tile_kt(const TileRange &r, int j)
@@ -107,12 +151,20 @@ int read_and_clear_status(cudaStream_t stream);
 // Launchers (each validates nothing: the public entry points do that).
 // ---------------------------------------------------------------------------
 // sink: per-head sink logits [H] (device, fp32) or null, for every launcher.
+// n: query rows (Q, O); n_k: key rows (K, V); pos0: device int32 [B] for a
+// chunked prefill over key lists (query t at index t + chunk_offset(pos0[b])),
+// or null for a plain prefill (n_k == n, query i at index i).
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
-                        const float *sink, int B, int H, int Hkv, int n, int d, int w, int g,
-                        float scale, cudaStream_t stream);
+                        const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
+                        int g, float scale, const int32_t *pos0, cudaStream_t stream);
 int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
-                       const float *sink, int B, int H, int Hkv, int n, int d, int w, int g,
-                       float scale, cudaStream_t stream);
+                       const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
+                       int g, float scale, const int32_t *pos0, cudaStream_t stream);
+// Builds the key lists of a chunked prefill: Kx, Vx [B][Hkv][rows][d] from
+// the rolling cache and the chunk; rows = chunk_rows_max(w, g, T).
+int launch_chunk_gather(void *Kx, void *Vx, const void *Kc, const void *Vc, const void *k_new,
+                        const void *v_new, const int32_t *pos0, int B, int Hkv, int T, int d,
+                        int w, int g, swa_dtype dt, cudaStream_t stream);
 // CTAs of the decode split pass: num_splits > 0 asks for about that many per
 // (sequence, kv head); 0 picks one resident wave on the current device.
 int decode_ctas(int B, int Hkv, int w, int g, int num_splits);

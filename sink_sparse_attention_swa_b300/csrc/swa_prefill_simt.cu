@@ -23,26 +23,36 @@ __global__ void __launch_bounds__(TM)
     swa_prefill_f32_simt(const float *__restrict__ Q, const float *__restrict__ K,
                          const float *__restrict__ V, float *__restrict__ O,
                          float *__restrict__ lse, const float *__restrict__ sink, int H,
-                         int Hkv, int n, int w, int g, float sl2)
+                         int Hkv, int n, int n_k, int w, int g, float sl2,
+                         const int32_t *__restrict__ pos0)
 {
     __shared__ __align__(16) float sK[TN][HD];
     __shared__ __align__(16) float sV[TN][HD];
     const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int kvh = h / (H / Hkv);
     const int r = threadIdx.x;
-    const int i = qt * TM + r;
-    const size_t qrow = (static_cast<size_t>(b) * H + h) * n + i;
-    const float *Kb = K + (static_cast<size_t>(b) * Hkv + kvh) * n * HD;
-    const float *Vb = V + (static_cast<size_t>(b) * Hkv + kvh) * n * HD;
+    // query row t of this thread; its index in the key list is i = t + off
+    // (a chunked prefill lists its keys from chunk_offset(pos0[b]) on)
+    int off = 0;
+    if (pos0 != nullptr) {
+        const int ps = pos0[b];
+        off = chunk_offset(ps < 0 ? 0 : ps, w, g);
+    }
+    const int t = qt * TM + r;
+    const int i = t + off;
+    const size_t qrow = (static_cast<size_t>(b) * H + h) * n + t;
+    const float *Kb = K + (static_cast<size_t>(b) * Hkv + kvh) * n_k * HD;
+    const float *Vb = V + (static_cast<size_t>(b) * Hkv + kvh) * n_k * HD;
 
     float q[HD], acc[HD];
 #pragma unroll
     for (int e = 0; e < HD; ++e) {
-        q[e] = (i < n) ? Q[qrow * HD + e] : 0.f;
+        q[e] = (t < n) ? Q[qrow * HD + e] : 0.f;
         acc[e] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
-    const TileRange tr = tile_range(qt, n, w, g, TM, TN);
+    const int q0 = qt * TM;
+    const TileRange tr = tile_range_at(q0 + off, (q0 + TM < n ? q0 + TM : n) - 1 + off, w, g, TN);
     const int lo = i - w + 1;
     for (int j = 0; j < tr.count; ++j) {
         const int k0 = tile_kt(tr, j) * TN;
@@ -51,7 +61,7 @@ __global__ void __launch_bounds__(TM)
             const int row = x / (HD / 4), c4 = x % (HD / 4);
             const int kk = k0 + row;
             float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-            if (kk < n) {
+            if (kk < n_k) {
                 kv = reinterpret_cast<const float4 *>(Kb + static_cast<size_t>(kk) * HD)[c4];
                 vv = reinterpret_cast<const float4 *>(Vb + static_cast<size_t>(kk) * HD)[c4];
             }
@@ -64,7 +74,7 @@ __global__ void __launch_bounds__(TM)
 #pragma unroll
         for (int c = 0; c < TN; ++c) {
             const int jj = k0 + c;
-            const bool allowed = (i < n) && (jj <= i) && (jj >= lo || jj < g);
+            const bool allowed = (t < n) && (jj <= i) && (jj >= lo || jj < g);
             float dot = 0.f;
 #pragma unroll
             for (int e = 0; e < HD; ++e) dot = fmaf(q[e], sK[c][e], dot);
@@ -86,7 +96,7 @@ __global__ void __launch_bounds__(TM)
         }
         m = m_new;
     }
-    if (i < n) {
+    if (t < n) {
         float row_lse;
         const float inv = finish_row(m, l, sink, h, &row_lse);
 #pragma unroll
@@ -97,24 +107,27 @@ __global__ void __launch_bounds__(TM)
 
 template <int HD>
 int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, const float *sink,
-              int B, int H, int Hkv, int n, int w, int g, float scale, cudaStream_t stream)
+              int B, int H, int Hkv, int n, int n_k, int w, int g, float scale,
+              const int32_t *pos0, cudaStream_t stream)
 {
     dim3 grid((n + TM - 1) / TM, H, B);
     swa_prefill_f32_simt<HD><<<grid, TM, 0, stream>>>(
         static_cast<const float *>(Q), static_cast<const float *>(K),
-        static_cast<const float *>(V), static_cast<float *>(O), lse, sink, H, Hkv, n, w, g,
-        scale * 1.4426950408889634f);
+        static_cast<const float *>(V), static_cast<float *>(O), lse, sink, H, Hkv, n, n_k, w, g,
+        scale * 1.4426950408889634f, pos0);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
 }  // namespace
 
 int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
-                       const float *sink, int B, int H, int Hkv, int n, int d, int w, int g,
-                       float scale, cudaStream_t stream)
+                       const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
+                       int g, float scale, const int32_t *pos0, cudaStream_t stream)
 {
-    if (d == 64) return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, w, g, scale, stream);
-    if (d == 128) return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, w, g, scale, stream);
+    if (d == 64)
+        return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, stream);
+    if (d == 128)
+        return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, stream);
     return SWA_ERR_UNSUPPORTED;
 }
 

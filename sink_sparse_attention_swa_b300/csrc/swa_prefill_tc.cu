@@ -85,6 +85,8 @@ struct Layout {
 
 struct PrefillParams {
     int B, H, Hkv, n, w, g, G, n_qt, num_items;
+    int n_k;                 // key rows (K, V); n is the query rows (Q, O)
+    const int32_t *pos0;     // chunked prefill: chunk start per sequence, or null
     float sl2;  // scale * log2(e)
     __nv_bfloat16 *O;
     float *lse;
@@ -102,6 +104,20 @@ __device__ __forceinline__ void decode_item(int t, const PrefillParams &p, int &
     kvh = t % p.Hkv;
     b = t / p.Hkv;
     h = kvh * p.G + hg;
+}
+
+// Key tiles of query tile qt of sequence b, in key-list indices; *off is the
+// list index of query row 0 (0 for a plain prefill, chunk_offset(pos0[b]) for
+// a chunked one).
+__device__ __forceinline__ TileRange item_tiles(const PrefillParams &p, int b, int qt, int &off)
+{
+    off = 0;
+    if (p.pos0 != nullptr) {
+        const int ps = __ldg(p.pos0 + b);
+        off = chunk_offset(ps < 0 ? 0 : ps, p.w, p.g);
+    }
+    const int q0 = qt * BM, q1 = (q0 + BM < p.n ? q0 + BM : p.n) - 1;
+    return tile_range_at(q0 + off, q1 + off, p.w, p.g, BN);
 }
 
 __device__ __forceinline__ float ex2(float x)
@@ -196,7 +212,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
                 int b, h, kvh, qt;
                 decode_item(t, p, b, h, kvh, qt);
-                const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+                int off;
+                const TileRange tr = item_tiles(p, b, qt, off);
                 for (int j = 0; j < tr.count; ++j, ++kv_iter) {
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
@@ -276,7 +293,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
                 int b, h, kvh, qt;
                 decode_item(t, p, b, h, kvh, qt);
-                const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+                int off;
+                const TileRange tr = item_tiles(p, b, qt, off);
                 const int qb = it & 1;
                 if (!warp_wait(BAR(L::Q_FULL + qb), (it >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
@@ -332,7 +350,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
             int b, h, kvh, qt;
             decode_item(t, p, b, h, kvh, qt);
-            const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+            int off;
+            const TileRange tr = item_tiles(p, b, qt, off);
             const int i = tr.q0 + r;
             const int lo = i - p.w + 1;
             float m = -INFINITY, l = 0.f;
@@ -450,7 +469,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_after();
             float row_lse;
             const float inv_l = finish_row(m, l, p.sink, h, &row_lse);
-            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + i) * HD;
+            const int t_row = i - off;  // the query row of this thread
+            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + t_row) * HD;
 #pragma unroll 1
             for (int q = 0; q < HD / 32; ++q) {
                 uint32_t o[32];
@@ -462,7 +482,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int e = 0; e < 16; ++e)
                     pkd[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
                                          __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (i < p.n) {
+                if (t_row < p.n) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
@@ -472,8 +492,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY));
-            if (p.lse != nullptr && i < p.n)
-                p.lse[static_cast<size_t>(b * p.H + h) * p.n + i] = row_lse;
+            if (p.lse != nullptr && t_row < p.n)
+                p.lse[static_cast<size_t>(b * p.H + h) * p.n + t_row] = row_lse;
         }
     }
 #undef BAR
@@ -505,10 +525,10 @@ constexpr int NTHREADS2 = 384;
 // named barriers 1 (head A) and 2 (head B): a softmax warpgroup's 128 threads
 // arrive when P is in tensor memory, the 32 threads of the MMA warp wait
 constexpr int P_BAR_THREADS = 128 + 32;
-// registers per thread after the hand-over: 128 * (56 + 224 + 224) equals the
+// registers per thread after the hand-over: 128 * (104 + 200 + 200) equals the
 // 384 * 168 registers the kernel is launched with
-constexpr int REGS_CTRL = 88;
-constexpr int REGS_SOFTMAX = 208;
+constexpr int REGS_CTRL = 104;
+constexpr int REGS_SOFTMAX = 200;
 
 template <int HD>
 struct Layout2 {
@@ -684,7 +704,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                  t = pair_item_rank(blockIdx.x, ++it)) {
                 int b, h0, kvh, qt;
                 decode_pair_item(t, p, b, h0, kvh, qt);
-                const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+                int off;
+                const TileRange tr = item_tiles(p, b, qt, off);
                 for (int x = 0; x < 2 && ok; ++x) {
                     if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
                                    TIMEOUT_NS)) {
@@ -789,7 +810,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                  t = pair_item_rank(blockIdx.x, ++it)) {
                 int b, h0, kvh, qt;
                 decode_pair_item(t, p, b, h0, kvh, qt);
-                const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+                int off;
+                const TileRange tr = item_tiles(p, b, qt, off);
                 for (int j = 0; j < tr.count; ++j, ++kv_iter, ++c) {
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
@@ -851,7 +873,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             int b, h0, kvh, qt;
             decode_pair_item(t, p, b, h0, kvh, qt);
             const int h = h0 + x;
-            const TileRange tr = tile_range(qt, p.n, p.w, p.g, BM, BN);
+            int off;
+            const TileRange tr = item_tiles(p, b, qt, off);
             const int i = tr.q0 + r;
             const int lo = i - p.w + 1;
             float m = -INFINITY, l = 0.f;
@@ -936,7 +959,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             tc_fence_after();
             float row_lse;
             const float inv_l = finish_row(m, l, p.sink, h, &row_lse);
-            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + i) * HD;
+            const int t_row = i - off;  // the query row of this thread
+            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + t_row) * HD;
 #pragma unroll 1
             for (int q = 0; q < HD / 32; ++q) {
                 uint32_t o[32];
@@ -948,7 +972,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 for (int e = 0; e < 16; ++e)
                     pkd[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
                                          __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (i < p.n) {
+                if (t_row < p.n) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
@@ -958,8 +982,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY + x));
-            if (p.lse != nullptr && i < p.n)
-                p.lse[static_cast<size_t>(b * p.H + h) * p.n + i] = row_lse;
+            if (p.lse != nullptr && t_row < p.n)
+                p.lse[static_cast<size_t>(b * p.H + h) * p.n + t_row] = row_lse;
         }
         // gave up (a wait ran out): one more arrival lets an issuer that is
         // already waiting for this head's P meet, see the abort flag and stop
@@ -1114,13 +1138,14 @@ bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
 
 template <int HD>
 int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, const float *sink,
-              int B, int H, int Hkv, int n, int w, int g, float scale, cudaStream_t stream)
+              int B, int H, int Hkv, int n, int n_k, int w, int g, float scale,
+              const int32_t *pos0, cudaStream_t stream)
 {
     using L = Layout<HD>;
     CUtensorMap mq, mk, mv;
     if (!make_map_3d(&mq, Q, HD, n, static_cast<uint64_t>(B) * H, BM) ||
-        !make_map_3d(&mk, K, HD, n, static_cast<uint64_t>(B) * Hkv, BN) ||
-        !make_map_3d(&mv, V, HD, n, static_cast<uint64_t>(B) * Hkv, BN))
+        !make_map_3d(&mk, K, HD, n_k, static_cast<uint64_t>(B) * Hkv, BN) ||
+        !make_map_3d(&mv, V, HD, n_k, static_cast<uint64_t>(B) * Hkv, BN))
         return SWA_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -1134,6 +1159,8 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     p.H = H;
     p.Hkv = Hkv;
     p.n = n;
+    p.n_k = n_k;
+    p.pos0 = pos0;
     p.w = w;
     p.g = g;
     p.G = H / Hkv;
@@ -1169,11 +1196,13 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
 }  // namespace
 
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
-                        const float *sink, int B, int H, int Hkv, int n, int d, int w, int g,
-                        float scale, cudaStream_t stream)
+                        const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
+                        int g, float scale, const int32_t *pos0, cudaStream_t stream)
 {
-    if (d == 128) return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, w, g, scale, stream);
-    if (d == 64) return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, w, g, scale, stream);
+    if (d == 128)
+        return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, stream);
+    if (d == 64)
+        return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, stream);
     return SWA_ERR_UNSUPPORTED;
 }
 

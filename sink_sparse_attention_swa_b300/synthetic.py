@@ -15,6 +15,9 @@ Workloads (the shapes come from the model families the pages quote):
                           sink keys (positions 0..3) scaled x4
   gemma3_global_prefill   B=2 H=32 Hkv=16 n=32768 d=128 w=n (full causal) g=0,
                           bf16: the global layer between the local ones
+  chunked_prefill_stream  B=4 H=32 Hkv=8 d=128 w=4096 g=4, a chunk of T=4096
+                          prompt tokens at positions 100000 .. 104095 against
+                          a full rolling cache (sink keys x4), bf16
 """
 from __future__ import annotations
 
@@ -36,6 +39,8 @@ WORKLOADS = {
                               g=4, dtype="bf16", sink_scale=4.0),
     "gemma3_global_prefill": dict(kind="prefill", B=2, H=32, Hkv=16, n=32768, d=128, w=32768,
                                   g=0, dtype="bf16", sink_scale=1.0),
+    "chunked_prefill_stream": dict(kind="chunk", B=4, H=32, Hkv=8, d=128, w=4096, g=4, T=4096,
+                                   pos0=100000, dtype="bf16", sink_scale=4.0),
 }
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
@@ -140,3 +145,37 @@ def sample_rows(B, H, n, count, seed=1):
     h = (idx // n) % H
     b = idx // (n * H)
     return torch.stack([b, h, i], dim=1).to(torch.int64)
+
+
+@dataclass
+class ChunkInputs:
+    q: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    Kc: torch.Tensor
+    Vc: torch.Tensor
+    pos0: torch.Tensor
+    w: int
+    g: int
+    scale: float
+
+
+def chunk_inputs(B, H, Hkv, d, w, g, T, pos0, dtype="bf16", seed=0, sink_scale=1.0,
+                 device="cpu", scale=None) -> ChunkInputs:
+    """A chunk of T tokens at positions pos0 .. pos0+T-1 (the same pos0 for every
+    sequence) against a filled rolling cache: the cache and the chunk's queries
+    come from decode_cache_inputs-style draws (Kc, Vc, then q [B,H,T,d]), the
+    chunk's keys and values from a second generator seeded seed+1 (k_new,
+    v_new [B,Hkv,T,d])."""
+    gen = _gen(seed, device)
+    S = w + g
+    Kc = torch.randn(B, Hkv, S, d, generator=gen, device=device, dtype=torch.float32)
+    Vc = torch.randn(B, Hkv, S, d, generator=gen, device=device, dtype=torch.float32)
+    q = torch.randn(B, H, T, d, generator=gen, device=device, dtype=torch.float32)
+    if g > 0 and sink_scale != 1.0:
+        Kc[:, :, w:] *= sink_scale
+    kn, vn = token_stream(B, Hkv, d, T, dtype=dtype, seed=seed + 1, device=device)
+    dt = torch_dtype(dtype)
+    pos_t = torch.full((B,), pos0, dtype=torch.int32, device=device)
+    return ChunkInputs(q.to(dt), kn, vn, Kc.to(dt), Vc.to(dt), pos_t, w, g,
+                       default_scale(d) if scale is None else scale)
