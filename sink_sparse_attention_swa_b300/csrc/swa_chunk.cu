@@ -8,10 +8,11 @@
 // kernel lays them out, per (sequence, kv head), in the order the prefill
 // kernels expect (swa_internal.h, chunk_*):
 //   rows 0 .. S-1        sink slots w .. w+S-1 (positions 0 .. S-1)
-//   rows S .. S+A-1      ring slots of positions W0 .. pos0-1 (A = pos0 - W0)
-//   rows S+A .. S+A+T-1  the chunk's own keys (positions pos0 .. pos0+T-1)
+//   rows S .. S+p-1      zero (the alignment padding, p = chunk_pad)
+//   rows S+p .. S+p+A-1  ring slots of positions W0 .. pos0-1 (A = pos0 - W0)
+//   then T rows          the chunk's own keys (positions pos0 .. pos0+T-1)
 //   the remaining rows   zero (never read by a valid query; zero so that the
-//                        padding rows of the last key tile hold finite values)
+//                        unused rows of a partial key tile hold finite values)
 // so the prefill kernels read each key with a 2-D tiled copy of contiguous
 // rows, whatever the ring's wrap-around.
 #include <cuda_bf16.h>
@@ -41,17 +42,17 @@ __global__ void swa_chunk_gather_k(T *__restrict__ Kx, T *__restrict__ Vx, const
             if (r == 0 && c == 0 && bk % Hkv == 0) atomicOr(status, DEV_ERR_BAD_POS);
             ps = 0;
         }
-        const int S = chunk_sinks(ps, g), W0 = chunk_w0(ps, w, g);
-        const int L = S + (ps - W0) + Tn;
+        const int S = chunk_sinks(ps, g), W0 = chunk_w0(ps, w, g), pad = chunk_pad(ps, w, g);
+        const int L = S + pad + (ps - W0) + Tn;
         uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
-        if (r < L) {
+        if (r < L && (r < S || r >= S + pad)) {
             const T *ks, *vs;
             if (r < S) {  // a sink slot
                 const size_t off = (bk * slots + w + r) * HD;
                 ks = Kc + off;
                 vs = Vc + off;
             } else {
-                const int pos = W0 + (r - S);
+                const int pos = W0 + (r - S - pad);
                 if (pos < ps) {  // still in the ring
                     const size_t off = (bk * slots + pos % w) * HD;
                     ks = Kc + off;

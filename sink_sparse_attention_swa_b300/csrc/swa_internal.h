@@ -69,23 +69,35 @@ __host__ __device__ inline TileRange tile_range(int qt, int n, int w, int g, int
 // chunk of T new tokens at positions pos0 .. pos0+T-1 attends to the rolling
 // cache and to itself.  Its keys are laid out as one list:
 //   indices 0 .. S-1        positions 0 .. S-1 (the sinks, S = min(g, pos0)),
-//   indices S ..            positions W0 .. pos0+T-1 (window part of the
+//   indices S .. S+pad-1    padding (zero rows no query reads),
+//   indices S+pad ..        positions W0 .. pos0+T-1 (window part of the
 //                           cache, then the chunk), W0 = max(S, pos0-w+1).
 // Positions S .. W0-1 are left out: no query of the chunk reads them.  Index
 // differences equal position differences after the sinks, and the sinks are
 // the first g indices (or all positions, when pos0 < g), so the prefill mask
 // (j <= i, j >= i-w+1 or j < g) holds on list indices with query t at index
-// t + chunk_offset.
+// t + chunk_offset.  The padding only exists once the window has moved past
+// the sinks (S = g and W0 = pos0-w+1 > g-1): then every padding index is
+// >= g and below the band of the chunk's first query, and pad makes
+// chunk_offset a multiple of the 128-row query tile, so the chunk's query
+// tiles meet the key tiles as aligned as in a plain prefill.
 // ---------------------------------------------------------------------------
+constexpr int CHUNK_ALIGN = 128;
 __host__ __device__ inline int chunk_sinks(int pos0, int g) { return pos0 < g ? pos0 : g; }
 __host__ __device__ inline int chunk_w0(int pos0, int w, int g)
 {
     const int s = chunk_sinks(pos0, g), a = pos0 - w + 1;
     return s > a ? s : a;
 }
+__host__ __device__ inline int chunk_pad(int pos0, int w, int g)
+{
+    if (pos0 < g || pos0 - w + 1 < g) return 0;
+    const int r = (g + w - 1) % CHUNK_ALIGN;
+    return r == 0 ? 0 : CHUNK_ALIGN - r;
+}
 __host__ __device__ inline int chunk_offset(int pos0, int w, int g)
 {
-    return pos0 + chunk_sinks(pos0, g) - chunk_w0(pos0, w, g);
+    return pos0 + chunk_sinks(pos0, g) + chunk_pad(pos0, w, g) - chunk_w0(pos0, w, g);
 }
 // rows of the key list for a chunk of T tokens at pos0
 __host__ __device__ inline int chunk_keys(int pos0, int w, int g, int T)
@@ -93,10 +105,11 @@ __host__ __device__ inline int chunk_keys(int pos0, int w, int g, int T)
     return chunk_offset(pos0, w, g) + T;
 }
 // the largest key list over all pos0, rounded up to whole 128-row tiles
+// (chunk_offset <= roundup(g + w - 1, 128))
 __host__ __device__ inline long long chunk_rows_max(int w, int g, int T)
 {
-    const long long m = static_cast<long long>(g) + (w - 1) + T;
-    return (m + 127) / 128 * 128;
+    const long long a = CHUNK_ALIGN;
+    return (static_cast<long long>(g) + w - 1 + a - 1) / a * a + (static_cast<long long>(T) + a - 1) / a * a;
 }
 
 __host__ __device__ inline int tile_kt(const TileRange &r, int j)

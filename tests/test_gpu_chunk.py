@@ -47,6 +47,8 @@ CASES = [
     (2, 3, 1, 128, 100, 2, 130, [1000, 99]),    # one-head kernel (odd group), T > one tile
     (2, 2, 2, 64, 37, 5, 1, [200, 5]),          # a single token (a decode step), d = 64
     (1, 8, 2, 128, 300, 3, 257, [600]),         # group of 4, ragged tiles
+    (2, 2, 1, 64, 1, 2, 40, [1, 10]),           # window one: only the token itself and sinks
+    (2, 4, 2, 128, 128, 0, 150, [300, 50]),     # no sinks, a window of one whole tile
 ]
 
 
