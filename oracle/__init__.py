@@ -61,6 +61,15 @@ def _load():
         lib.oracle_decode_history.argtypes = [_ptr] * 4 + [_i64] * 7 + [_dbl, _ptr, _ptr, _ptr]
         lib.oracle_cache_slots.argtypes = [_i64, _i64, _i64, _ptr, _ptr]
         lib.oracle_decode_cache.argtypes = [_ptr] * 4 + [_i64] * 6 + [_dbl, _ptr, _ptr, _ptr]
+        lib.oracle_pattern_mask_row.argtypes = [_i64] * 5 + [ctypes.c_int, _ptr]
+        lib.oracle_pattern_mask.argtypes = [_i64] * 4 + [ctypes.c_int, _ptr]
+        lib.oracle_pattern_count_pairs.argtypes = [_i64] * 4 + [ctypes.c_int]
+        lib.oracle_pattern_count_pairs.restype = _i64
+        lib.oracle_prefill_pattern.argtypes = ([_ptr] * 5 + [_i64] * 8 +
+                                               [ctypes.c_int, _dbl, _ptr])
+        lib.oracle_prefill_pattern_rows.argtypes = ([_ptr] * 3 + [_i64] * 8 +
+                                                    [ctypes.c_int, _dbl, _ptr, _i64, _ptr, _ptr,
+                                                     _ptr])
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -114,6 +123,61 @@ def mask(n: int, w: int, g: int) -> np.ndarray:
 
 def count_pairs(n: int, w: int, g: int) -> int:
     return int(_load().oracle_count_pairs(n, w, g))
+
+
+# Fixed patterns (see oracle_pattern_mask_row in the C source).
+PATTERNS = {"window": 0, "dilated": 1, "strided": 2, "landmark": 3}
+
+
+def _pat(pattern) -> int:
+    return PATTERNS[pattern] if isinstance(pattern, str) else int(pattern)
+
+
+def pattern_mask_row(i: int, n: int, w: int, g: int, r: int, pattern) -> np.ndarray:
+    row = np.zeros(n, dtype=np.uint8)
+    _load().oracle_pattern_mask_row(i, n, w, g, r, _pat(pattern), _p(row))
+    return row
+
+
+def pattern_mask(n: int, w: int, g: int, r: int, pattern) -> np.ndarray:
+    m = np.zeros((n, n), dtype=np.uint8)
+    _load().oracle_pattern_mask(n, w, g, r, _pat(pattern), _p(m))
+    return m
+
+
+def pattern_count_pairs(n: int, w: int, g: int, r: int, pattern) -> int:
+    return int(_load().oracle_pattern_count_pairs(n, w, g, r, _pat(pattern)))
+
+
+def prefill_pattern(Q, K, V, w: int, g: int, r: int, pattern, scale: float, sink_logit=None):
+    """prefill() under a fixed pattern (window, dilated, strided, landmark)."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, n, d = Q.shape
+    Hkv = K.shape[1]
+    assert K.shape == (B, Hkv, n, d) and V.shape == K.shape and H % Hkv == 0
+    O = np.empty_like(Q)
+    L = np.empty((B, H, n), dtype=np.float64)
+    sl = _sinks(sink_logit, H)
+    _load().oracle_prefill_pattern(_p(Q), _p(K), _p(V), _p(O), _p(L), B, H, Hkv, n, d, w, g, r,
+                                   _pat(pattern), float(scale), _pn(sl))
+    return O, L
+
+
+def prefill_pattern_rows(q_rows, K, V, H: int, w: int, g: int, r: int, pattern, scale: float,
+                         rows, sink_logit=None):
+    """prefill_rows() under a fixed pattern."""
+    q_rows, K, V = _f64(q_rows), _f64(K), _f64(V)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    B, Hkv, n, d = K.shape
+    m = rows.shape[0]
+    assert rows.shape == (m, 3) and q_rows.shape == (m, d)
+    O = np.empty((m, d), dtype=np.float64)
+    L = np.empty(m, dtype=np.float64)
+    sl = _sinks(sink_logit, H)
+    _load().oracle_prefill_pattern_rows(_p(q_rows), _p(K), _p(V), B, H, Hkv, n, d, w, g, r,
+                                        _pat(pattern), float(scale), _p(rows), m, _p(O), _p(L),
+                                        _pn(sl))
+    return O, L
 
 
 def tiles(n: int, w: int, g: int, BM: int, BN: int) -> np.ndarray:

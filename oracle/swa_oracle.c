@@ -156,6 +156,93 @@ void oracle_tiles(int64_t n, int64_t w, int64_t g, int64_t BM, int64_t BN, int32
 }
 
 /* ------------------------------------------------------------------------ */
+/* Other fixed patterns.                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Pattern codes (the same numbers as the library's public enum, which this
+ * file does not include):
+ *   0  window     the band of the last w cells plus the sinks (above);
+ *   1  dilated    every r-th key in a band r times wider: the keys i, i-r,
+ *                 ..., i-(w-1)r ([SW] §2 "Dilated windows": the cost of a
+ *                 window of w, a reach r times longer; [SW] §10 glossary:
+ *                 a window that attends to every r-th key);
+ *   2  strided    the Sparse Transformer's strided head: every j with
+ *                 (i - j) mod r = 0 ([SW] §4, Sparse Transformer);
+ *   3  landmark   the band of the last w cells plus positions designated at
+ *                 regular intervals, j mod r = 0 ([LS] Fig. 2, right: with
+ *                 w = 3 and r = 4, position 7 reads 0, 4, 5, 6, 7).
+ * In every pattern the sink columns j < g are added where causal, and no key
+ * is read twice (a mask is a set).
+ */
+void oracle_pattern_mask_row(int64_t i, int64_t n, int64_t w, int64_t g, int64_t r,
+                             int pattern, uint8_t *row)
+{
+    int64_t j;
+    if (pattern == 0) {
+        oracle_mask_row(i, n, w, g, row);
+        return;
+    }
+    /* causal triangle */
+    for (j = 0; j < n; ++j)
+        row[j] = (uint8_t)(j <= i);
+    if (pattern == 1 || pattern == 2) {
+        /* only keys a whole number of strides back */
+        for (j = 0; j < n; ++j)
+            if ((i - j) % r != 0)
+                row[j] = 0;
+        /* dilated: only the w nearest of them */
+        if (pattern == 1)
+            for (j = 0; j < n; ++j)
+                if (i - j > (w - 1) * r)
+                    row[j] = 0;
+    } else if (pattern == 3) {
+        /* the band of the last w cells ... */
+        for (j = 0; j < n; ++j)
+            if (j < i - w + 1)
+                row[j] = 0;
+        /* ... plus the landmark positions, where causal */
+        for (j = 0; j < n; j += r)
+            if (j <= i)
+                row[j] = 1;
+    }
+    /* the sink columns, where causal */
+    for (j = 0; j < n && j < g; ++j)
+        if (j <= i)
+            row[j] = 1;
+}
+
+/* The whole n x n mask of a pattern, row-major (n*n bytes, caller-owned). */
+void oracle_pattern_mask(int64_t n, int64_t w, int64_t g, int64_t r, int pattern, uint8_t *mask)
+{
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < n; ++i)
+        oracle_pattern_mask_row(i, n, w, g, r, pattern, mask + (size_t)i * (size_t)n);
+}
+
+/* The number of connections of a pattern: the count of ones in its mask. */
+int64_t oracle_pattern_count_pairs(int64_t n, int64_t w, int64_t g, int64_t r, int pattern)
+{
+    int64_t total = 0;
+#pragma omp parallel reduction(+ : total)
+    {
+        uint8_t *row = (uint8_t *)malloc((size_t)(n > 0 ? n : 1));
+        int64_t ii;
+#pragma omp for schedule(static)
+        for (ii = 0; ii < n; ++ii) {
+            int64_t j, c = 0;
+            oracle_pattern_mask_row(ii, n, w, g, r, pattern, row);
+            for (j = 0; j < n; ++j)
+                c += row[j];
+            total += c;
+        }
+        free(row);
+    }
+    return total;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Attention.                                                                */
 /* ------------------------------------------------------------------------ */
 
@@ -276,6 +363,64 @@ void oracle_prefill_rows(const double *q_rows, const double *K, const double *V,
             oracle_mask_row(i, n, w, g, mrow);
             attend_row(q, Kbh, Vbh, mrow, n, d, scale, 0, sink_of(sink_logits, h), s,
                        O_rows + t * d, LSE_rows ? LSE_rows + t : NULL);
+        }
+        free(mrow);
+        free(s);
+    }
+}
+
+/*
+ * Prefill under one of the fixed patterns above (pattern 0 is oracle_prefill
+ * itself).  Same layouts and arithmetic as oracle_prefill; only the mask row
+ * differs.
+ */
+void oracle_prefill_pattern(const double *Q, const double *K, const double *V, double *O,
+                            double *LSE, int64_t B, int64_t H, int64_t Hkv, int64_t n,
+                            int64_t d, int64_t w, int64_t g, int64_t r, int pattern,
+                            double scale, const double *sink_logits)
+{
+    int64_t t, rows = B * H * n, G = H / Hkv;
+#pragma omp parallel
+    {
+        uint8_t *mrow = (uint8_t *)malloc((size_t)(n > 0 ? n : 1));
+        double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (t = 0; t < rows; ++t) {
+            int64_t i = t % n, h = (t / n) % H, b = t / (n * H);
+            int64_t kvh = h / G;
+            const double *Kbh = K + ((b * Hkv + kvh) * n) * d;
+            const double *Vbh = V + ((b * Hkv + kvh) * n) * d;
+            oracle_pattern_mask_row(i, n, w, g, r, pattern, mrow);
+            attend_row(Q + t * d, Kbh, Vbh, mrow, n, d, scale, 0, sink_of(sink_logits, h), s,
+                       O + t * d, LSE ? LSE + t : NULL);
+        }
+        free(mrow);
+        free(s);
+    }
+}
+
+/* oracle_prefill_rows under a fixed pattern: sampled (b, h, i) rows only. */
+void oracle_prefill_pattern_rows(const double *q_rows, const double *K, const double *V,
+                                 int64_t B, int64_t H, int64_t Hkv, int64_t n, int64_t d,
+                                 int64_t w, int64_t g, int64_t r, int pattern, double scale,
+                                 const int64_t *rows, int64_t nrows, double *O_rows,
+                                 double *LSE_rows, const double *sink_logits)
+{
+    int64_t t, G = H / Hkv;
+    (void)B;
+#pragma omp parallel
+    {
+        uint8_t *mrow = (uint8_t *)malloc((size_t)(n > 0 ? n : 1));
+        double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (t = 0; t < nrows; ++t) {
+            int64_t b = rows[3 * t], h = rows[3 * t + 1], i = rows[3 * t + 2];
+            int64_t kvh = h / G;
+            const double *Kbh = K + ((b * Hkv + kvh) * n) * d;
+            const double *Vbh = V + ((b * Hkv + kvh) * n) * d;
+            oracle_pattern_mask_row(i, n, w, g, r, pattern, mrow);
+            attend_row(q_rows + t * d, Kbh, Vbh, mrow, n, d, scale, 0, sink_of(sink_logits, h),
+                       s, O_rows + t * d, LSE_rows ? LSE_rows + t : NULL);
         }
         free(mrow);
         free(s);
