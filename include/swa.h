@@ -61,6 +61,14 @@ typedef enum {
 
 typedef enum { SWA_BF16 = 0, SWA_F32 = 1 } swa_dtype;
 
+/* Fixed attention patterns (swa_prefill_pattern). */
+typedef enum {
+    SWA_PATTERN_WINDOW = 0,   /* the last w positions plus the sinks 0..g-1       */
+    SWA_PATTERN_DILATED = 1,  /* positions i, i-r, ..., i-(w-1)r                  */
+    SWA_PATTERN_STRIDED = 2,  /* every position j <= i with (i - j) mod r == 0    */
+    SWA_PATTERN_LANDMARK = 3  /* the window and sinks plus every j <= i, j mod r == 0 */
+} swa_pattern;
+
 /* ---------------------------------------------------------------------- */
 /* Prefill: the whole prompt at once, block-sparse over BMxBN tiles.       */
 /* ---------------------------------------------------------------------- */
@@ -103,6 +111,34 @@ int swa_prefill_ex(const void *Q, const void *K, const void *V, void *O, float *
 int swa_prefill_sink_logit(const void *Q, const void *K, const void *V, void *O, float *lse,
                            const float *sink_logit, int B, int H, int Hkv, int n, int d, int w,
                            int g, float scale, swa_dtype dtype, swa_stream_t stream);
+
+/*
+ * swa_prefill_pattern -- prefill under another fixed pattern, with the
+ * layouts, outputs and sink logit of swa_prefill_sink_logit.  For query
+ * position i the allowed keys j <= i are:
+ *   SWA_PATTERN_WINDOW    i-w+1 <= j or j < g (swa_prefill_sink_logit itself;
+ *                         r is ignored);
+ *   SWA_PATTERN_DILATED   j = i - k r for k = 0 .. w-1 ("Sliding Window and
+ *                         Sparse Attention, from Longformer to CSA2", section
+ *                         2, dilated windows: the cost of a window of w, a
+ *                         reach r times longer);
+ *   SWA_PATTERN_STRIDED   (i - j) mod r == 0 (same page, section 4: the
+ *                         Sparse Transformer's strided head; w is ignored);
+ *   SWA_PATTERN_LANDMARK  i-w+1 <= j, or j < g, or j mod r == 0 ("Local and
+ *                         Sparse Attention: Reading Fewer Token Positions",
+ *                         Figure 2, right: positions designated at regular
+ *                         intervals, each key read once).
+ * r >= 1.  The dilated and strided patterns take no sinks: g must be 0
+ * (SWA_ERR_UNSUPPORTED otherwise).  Both run as R = r independent prefills,
+ * one per residue class i mod r, each over its own subsequence of rows; the
+ * landmark pattern adds, per 128-row query tile, the key tiles of the
+ * landmark positions that lie before its band.  Same dtypes and error
+ * behaviour as swa_prefill_sink_logit.
+ */
+int swa_prefill_pattern(const void *Q, const void *K, const void *V, void *O, float *lse,
+                        const float *sink_logit, int B, int H, int Hkv, int n, int d,
+                        swa_pattern pattern, int w, int g, int r, float scale, swa_dtype dtype,
+                        swa_stream_t stream);
 
 /*
  * swa_prefill_chunk -- chunked prefill into the rolling cache: T new tokens

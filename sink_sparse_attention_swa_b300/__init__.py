@@ -20,7 +20,8 @@ import os
 import torch
 
 __all__ = [
-    "SwaError", "prefill", "prefill_chunk", "decode", "cache_append", "decode_workspace_bytes",
+    "SwaError", "prefill", "prefill_pattern", "prefill_chunk", "prefill_chunk_workspace_bytes",
+    "PATTERNS", "decode", "cache_append", "decode_workspace_bytes",
     "count_pairs", "enumerate_tiles", "cache_slot", "device_status", "selftest_umma",
     "library_path", "lib",
 ]
@@ -31,6 +32,8 @@ _LIB_PATH = os.environ.get("SWA_LIBRARY", os.path.join(_PKG, "libswa.so"))
 STATUS = {0: "SWA_OK", -1: "SWA_ERR_INVALID_ARG", -2: "SWA_ERR_UNSUPPORTED", -3: "SWA_ERR_CUDA",
           -4: "SWA_ERR_DEVICE_TIMEOUT", -5: "SWA_ERR_ALLOC", -6: "SWA_ERR_WORKSPACE"}
 SWA_BF16, SWA_F32 = 0, 1
+# fixed patterns of swa_prefill_pattern
+PATTERNS = {"window": 0, "dilated": 1, "strided": 2, "landmark": 3}
 _DT = {torch.bfloat16: SWA_BF16, torch.float32: SWA_F32}
 
 # Every function the C header declares, with its ctypes signature.
@@ -39,6 +42,7 @@ SIGNATURES = {
     "swa_prefill": (_i, [_p, _p, _p, _p] + [_i] * 7 + [_f, _p]),
     "swa_prefill_ex": (_i, [_p, _p, _p, _p, _p] + [_i] * 7 + [_f, _i, _p]),
     "swa_prefill_sink_logit": (_i, [_p, _p, _p, _p, _p, _p] + [_i] * 7 + [_f, _i, _p]),
+    "swa_prefill_pattern": (_i, [_p] * 6 + [_i] * 5 + [_i] * 4 + [_f, _i, _p]),
     "swa_prefill_chunk_workspace_bytes": (_sz, [_i] * 7),
     "swa_prefill_chunk": (_i, [_p] * 9 + [_i] * 7 + [_f, _i, _i, _p, _sz, _p]),
     "swa_decode": (_i, [_p, _p, _p, _p] + [_i] * 6 + [_f, _p, _p]),
@@ -149,6 +153,36 @@ def prefill(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None, l
     rc = _load().swa_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, n, d,
                             int(w), int(g), scale, _DT[q.dtype], _stream(stream, q.device))
     _check("swa_prefill_ex", rc)
+    return out
+
+
+def prefill_pattern(q, k, v, pattern: str, w: int = 1, g: int = 0, r: int = 1,
+                    scale: float | None = None, out=None, lse=None, sink_logit=None, stream=None):
+    """Prefill under a fixed pattern (swa_prefill_pattern): "window" (w, g),
+    "dilated" (keys i, i-r, ..., i-(w-1)r), "strided" (every j with (i-j) mod r
+    == 0) or "landmark" (the window and sinks plus every j with j mod r == 0).
+    Shapes and dtypes as prefill()."""
+    _need(q, "q")
+    B, H, n, d = q.shape
+    Hkv = k.shape[1]
+    _need(k, "k", q.dtype, (B, Hkv, n, d))
+    _need(v, "v", q.dtype, (B, Hkv, n, d))
+    if q.dtype not in _DT:
+        raise TypeError("q must be bfloat16 or float32")
+    if pattern not in PATTERNS:
+        raise ValueError(f"pattern must be one of {sorted(PATTERNS)}")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, n))
+    if sink_logit is not None:
+        _need(sink_logit, "sink_logit", torch.float32, (H,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = _load().swa_prefill_pattern(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                     _ptr(sink_logit), B, H, Hkv, n, d, PATTERNS[pattern], int(w),
+                                     int(g), int(r), scale, _DT[q.dtype], _stream(stream, q.device))
+    _check("swa_prefill_pattern", rc)
     return out
 
 

@@ -53,10 +53,55 @@ int swa_prefill_sink_logit(const void *Q, const void *K, const void *V, void *O,
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == SWA_BF16)
         return launch_prefill_bf16(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, w, g, scale,
-                                   nullptr, st);
+                                   nullptr, 1, 0, st);
     if (dtype == SWA_F32)
         return launch_prefill_f32(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, w, g, scale,
-                                  nullptr, st);
+                                  nullptr, 1, 0, st);
+    return SWA_ERR_INVALID_ARG;
+}
+
+int swa_prefill_pattern(const void *Q, const void *K, const void *V, void *O, float *lse,
+                        const float *sink_logit, int B, int H, int Hkv, int n, int d,
+                        swa_pattern pattern, int w, int g, int r, float scale, swa_dtype dtype,
+                        swa_stream_t stream)
+{
+    if (pattern == SWA_PATTERN_WINDOW)
+        return swa_prefill_sink_logit(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, d, w, g, scale,
+                                      dtype, stream);
+    if (pattern != SWA_PATTERN_DILATED && pattern != SWA_PATTERN_STRIDED &&
+        pattern != SWA_PATTERN_LANDMARK)
+        return SWA_ERR_INVALID_ARG;
+    if (r < 1 || n < 1 || n > INT32_MAX - 256) return SWA_ERR_INVALID_ARG;
+    if (pattern == SWA_PATTERN_STRIDED) w = n;  // no limit on the number of strides back
+    int rc = check_heads(B, H, Hkv, d, w, g);
+    if (rc != SWA_OK) return rc;
+    // residue classes carry no sink columns (a sink below g belongs to one class only)
+    if (pattern != SWA_PATTERN_LANDMARK && g != 0) return SWA_ERR_UNSUPPORTED;
+    if (!scale_ok(scale)) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SWA_ERR_INVALID_ARG;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
+    if (sink_logit != nullptr && (reinterpret_cast<uintptr_t>(sink_logit) & 3u))
+        return SWA_ERR_INVALID_ARG;
+    int R = 1, rl = 0, wk = w;
+    if (pattern == SWA_PATTERN_LANDMARK) {
+        rl = r;
+    } else {
+        R = r < n ? r : n;  // strides past the sequence: each class is one row
+        const int rows = (n + R - 1) / R;
+        if (pattern == SWA_PATTERN_STRIDED || wk > rows) wk = rows;
+    }
+    const long long n_hi = (n + R - 1) / R;
+    // work items (tensor-core kernels) and CTAs (fp32 kernel) stay below 2^31
+    if (static_cast<long long>(B) * H * (((n_hi + 127) / 128) * R) > INT32_MAX ||
+        ((n_hi + 63) / 64) * R > INT32_MAX)
+        return SWA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == SWA_BF16)
+        return launch_prefill_bf16(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, wk, g, scale,
+                                   nullptr, R, rl, st);
+    if (dtype == SWA_F32)
+        return launch_prefill_f32(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, wk, g, scale,
+                                  nullptr, R, rl, st);
     return SWA_ERR_INVALID_ARG;
 }
 
@@ -105,9 +150,9 @@ int swa_prefill_chunk(const void *Q, const void *k_new, const void *v_new, void 
     }
     if (dtype == SWA_BF16)
         return launch_prefill_bf16(Q, Kx, Vx, O, lse, sink_logit, B, H, Hkv, T,
-                                   static_cast<int>(rows), d, w, g, scale, pos0, st);
+                                   static_cast<int>(rows), d, w, g, scale, pos0, 1, 0, st);
     return launch_prefill_f32(Q, Kx, Vx, O, lse, sink_logit, B, H, Hkv, T, static_cast<int>(rows),
-                              d, w, g, scale, pos0, st);
+                              d, w, g, scale, pos0, 1, 0, st);
 }
 
 int swa_prefill_ex(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,

@@ -30,9 +30,11 @@ namespace swa {
 // ---------------------------------------------------------------------------
 struct TileRange {
     int q0, q1;   // first and last existing query row of the tile
-    int ns;       // number of sink-only key tiles (visited first: 0 .. ns-1)
+    int nl;       // landmark key tiles (visited first: lt0 .. lt0+nl-1), see add_landmarks
+    int lt0;
+    int ns;       // number of sink-only key tiles (visited next: 0 .. ns-1)
     int kt_lo;    // first band key tile
-    int count;    // total key tiles visited
+    int count;    // total key tiles visited (nl + ns + band tiles)
 };
 
 // The key tiles for query rows q0 .. q1 (indices into the key list; any
@@ -42,6 +44,8 @@ __host__ __device__ inline TileRange tile_range_at(int q0, int q1, int w, int g,
     TileRange r;
     r.q0 = q0;
     r.q1 = q1;
+    r.nl = 0;
+    r.lt0 = 0;
     int lo = r.q0 - w + 1;
     if (lo < 0) lo = 0;
     r.kt_lo = lo / BN;
@@ -112,6 +116,34 @@ __host__ __device__ inline long long chunk_rows_max(int w, int g, int T)
     return (static_cast<long long>(g) + w - 1 + a - 1) / a * a + (static_cast<long long>(T) + a - 1) / a * a;
 }
 
+// ---------------------------------------------------------------------------
+// Landmarks ("Local and Sparse Attention: Reading Fewer Token Positions",
+// Figure 2, right): besides the band and the sinks, a query i reads every
+// position j = rl * m <= i.  A landmark inside the band is read there, one
+// below g as a sink, so the landmark tiles carry only the rest:
+//     g <= rl * m <= i - w,  i.e.  land_lo <= m <= land_hi(i),
+// with m the index into the landmark list (positions 0, rl, 2 rl, ...), which
+// the kernels load as dense 128-row tiles through a view of K and V whose row
+// stride is rl rows.  Landmark tiles are visited before the sink and band
+// tiles.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline int land_lo(int g, int rl) { return (g + rl - 1) / rl; }
+__host__ __device__ inline int land_hi(int i, int w, int rl) { return i >= w ? (i - w) / rl : -1; }
+__host__ __device__ inline void add_landmarks(TileRange &r, int w, int g, int rl, int BN)
+{
+    if (rl <= 0) return;
+    const int a = land_lo(g, rl), z = land_hi(r.q1, w, rl);
+    if (z < a) return;
+    r.lt0 = a / BN;
+    r.nl = z / BN - r.lt0 + 1;
+    r.count += r.nl;
+}
+// every landmark of tile lt is read by every row of the tile
+__host__ __device__ inline bool land_full(const TileRange &r, int lt, int w, int g, int rl, int BN)
+{
+    return lt * BN >= land_lo(g, rl) && lt * BN + BN - 1 <= land_hi(r.q0, w, rl);
+}
+
 __host__ __device__ inline int tile_kt(const TileRange &r, int j)
 {
     return j < r.ns ? j : r.kt_lo + (j - r.ns);
@@ -167,12 +199,22 @@ int read_and_clear_status(cudaStream_t stream);
 // n: query rows (Q, O); n_k: key rows (K, V); pos0: device int32 [B] for a
 // chunked prefill over key lists (query t at index t + chunk_offset(pos0[b])),
 // or null for a plain prefill (n_k == n, query i at index i).
+// R, rl: the fixed pattern (R = 1, rl = 0 for the window and sinks).
+//   R > 1   residue classes: query i and key j meet only when i = j (mod R),
+//           and each class c (positions c, c+R, c+2R, ...) is a window
+//           prefill of its own over that subsequence (the dilated pattern;
+//           the strided one is the same with w >= ceil(n/R)); needs n_k == n,
+//           pos0 == null, g == 0.
+//   rl > 0  landmarks every rl positions (add_landmarks); needs R == 1 and
+//           pos0 == null.
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
                         const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
-                        int g, float scale, const int32_t *pos0, cudaStream_t stream);
+                        int g, float scale, const int32_t *pos0, int R, int rl,
+                        cudaStream_t stream);
 int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
                        const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
-                       int g, float scale, const int32_t *pos0, cudaStream_t stream);
+                       int g, float scale, const int32_t *pos0, int R, int rl,
+                       cudaStream_t stream);
 // Builds the key lists of a chunked prefill: Kx, Vx [B][Hkv][rows][d] from
 // the rolling cache and the chunk; rows = chunk_rows_max(w, g, T).
 int launch_chunk_gather(void *Kx, void *Vx, const void *Kc, const void *Vc, const void *k_new,

@@ -5,9 +5,11 @@
 //
 // ("Sliding Window and Sparse Attention, from Longformer to CSA2", sections
 // 1-2; "Local and Sparse Attention: Reading Fewer Token Positions", Figures
-// 1-2.)  One CTA per (q tile of 64 rows, head, batch); one query row per
-// thread; key/value tiles of 32 rows staged in shared memory; online softmax
-// in base 2 with the scale folded in.
+// 1-2.)  One CTA per (q tile of 64 rows, residue class, head, batch); one
+// query row per thread; key/value tiles of 32 rows staged in shared memory;
+// online softmax in base 2 with the scale folded in.  The fixed patterns run
+// as in the tensor-core kernel: residue classes (R > 1) address rows c + R t
+// of class c; landmark tiles (rl > 0) read the rows 0, rl, 2 rl, ... .
 #include <cmath>
 
 #include "swa_internal.h"
@@ -24,13 +26,17 @@ __global__ void __launch_bounds__(TM)
                          const float *__restrict__ V, float *__restrict__ O,
                          float *__restrict__ lse, const float *__restrict__ sink, int H,
                          int Hkv, int n, int n_k, int w, int g, float sl2,
-                         const int32_t *__restrict__ pos0)
+                         const int32_t *__restrict__ pos0, int R, int rl)
 {
     __shared__ __align__(16) float sK[TN][HD];
     __shared__ __align__(16) float sV[TN][HD];
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int cls = blockIdx.x % R, qt = blockIdx.x / R, h = blockIdx.y, b = blockIdx.z;
     const int kvh = h / (H / Hkv);
     const int r = threadIdx.x;
+    // rows (and keys) of this class: indices into its subsequence c, c+R, ...
+    const int nq = (n - cls + R - 1) / R;
+    const int nk = R == 1 ? n_k : nq;
+    if (qt * TM >= nq) return;  // a class one row short may have one tile less
     // query row t of this thread; its index in the key list is i = t + off
     // (a chunked prefill lists its keys from chunk_offset(pos0[b]) on)
     int off = 0;
@@ -40,30 +46,38 @@ __global__ void __launch_bounds__(TM)
     }
     const int t = qt * TM + r;
     const int i = t + off;
-    const size_t qrow = (static_cast<size_t>(b) * H + h) * n + t;
+    const size_t qrow = (static_cast<size_t>(b) * H + h) * n + cls + static_cast<size_t>(R) * t;
     const float *Kb = K + (static_cast<size_t>(b) * Hkv + kvh) * n_k * HD;
     const float *Vb = V + (static_cast<size_t>(b) * Hkv + kvh) * n_k * HD;
 
     float q[HD], acc[HD];
 #pragma unroll
     for (int e = 0; e < HD; ++e) {
-        q[e] = (t < n) ? Q[qrow * HD + e] : 0.f;
+        q[e] = (t < nq) ? Q[qrow * HD + e] : 0.f;
         acc[e] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
     const int q0 = qt * TM;
-    const TileRange tr = tile_range_at(q0 + off, (q0 + TM < n ? q0 + TM : n) - 1 + off, w, g, TN);
+    TileRange tr = tile_range_at(q0 + off, (q0 + TM < nq ? q0 + TM : nq) - 1 + off, w, g, TN);
+    add_landmarks(tr, w, g, rl, TN);
     const int lo = i - w + 1;
+    const int lhi = land_hi(i, w, rl > 0 ? rl : 1), llo = rl > 0 ? land_lo(g, rl) : 0;
     for (int j = 0; j < tr.count; ++j) {
-        const int k0 = tile_kt(tr, j) * TN;
+        // landmark tiles first (k a landmark index, key row rl k), then the
+        // sink and band tiles (k an index into the class, key row c + R k)
+        const bool land = j < tr.nl;
+        const int k0 = (land ? tr.lt0 + j : tile_kt(tr, j - tr.nl)) * TN;
+        const int khi = land ? lhi : i, klo = land ? llo : lo, kgs = land ? 0 : g;
         __syncthreads();
         for (int x = r; x < TN * HD / 4; x += TM) {
             const int row = x / (HD / 4), c4 = x % (HD / 4);
             const int kk = k0 + row;
+            const long long krow = land ? static_cast<long long>(rl) * kk
+                                        : cls + static_cast<long long>(R) * kk;
             float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-            if (kk < n_k) {
-                kv = reinterpret_cast<const float4 *>(Kb + static_cast<size_t>(kk) * HD)[c4];
-                vv = reinterpret_cast<const float4 *>(Vb + static_cast<size_t>(kk) * HD)[c4];
+            if (land ? krow < n_k : kk < nk) {
+                kv = reinterpret_cast<const float4 *>(Kb + static_cast<size_t>(krow) * HD)[c4];
+                vv = reinterpret_cast<const float4 *>(Vb + static_cast<size_t>(krow) * HD)[c4];
             }
             reinterpret_cast<float4 *>(&sK[row][0])[c4] = kv;
             reinterpret_cast<float4 *>(&sV[row][0])[c4] = vv;
@@ -74,7 +88,7 @@ __global__ void __launch_bounds__(TM)
 #pragma unroll
         for (int c = 0; c < TN; ++c) {
             const int jj = k0 + c;
-            const bool allowed = (t < n) && (jj <= i) && (jj >= lo || jj < g);
+            const bool allowed = (t < nq) && (jj <= khi) && (jj >= klo || jj < kgs);
             float dot = 0.f;
 #pragma unroll
             for (int e = 0; e < HD; ++e) dot = fmaf(q[e], sK[c][e], dot);
@@ -96,7 +110,7 @@ __global__ void __launch_bounds__(TM)
         }
         m = m_new;
     }
-    if (t < n) {
+    if (t < nq) {
         float row_lse;
         const float inv = finish_row(m, l, sink, h, &row_lse);
 #pragma unroll
@@ -108,13 +122,15 @@ __global__ void __launch_bounds__(TM)
 template <int HD>
 int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, const float *sink,
               int B, int H, int Hkv, int n, int n_k, int w, int g, float scale,
-              const int32_t *pos0, cudaStream_t stream)
+              const int32_t *pos0, int R, int rl, cudaStream_t stream)
 {
-    dim3 grid((n + TM - 1) / TM, H, B);
+    if (rl > 0) R = 1;
+    const int n_hi = (n + R - 1) / R;
+    dim3 grid(((n_hi + TM - 1) / TM) * R, H, B);
     swa_prefill_f32_simt<HD><<<grid, TM, 0, stream>>>(
         static_cast<const float *>(Q), static_cast<const float *>(K),
         static_cast<const float *>(V), static_cast<float *>(O), lse, sink, H, Hkv, n, n_k, w, g,
-        scale * 1.4426950408889634f, pos0);
+        scale * 1.4426950408889634f, pos0, R, rl);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
@@ -122,12 +138,15 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
 
 int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
                        const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
-                       int g, float scale, const int32_t *pos0, cudaStream_t stream)
+                       int g, float scale, const int32_t *pos0, int R, int rl,
+                       cudaStream_t stream)
 {
     if (d == 64)
-        return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, stream);
+        return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
+                             stream);
     if (d == 128)
-        return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, stream);
+        return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
+                              stream);
     return SWA_ERR_UNSUPPORTED;
 }
 

@@ -87,6 +87,11 @@ struct PrefillParams {
     int B, H, Hkv, n, w, g, G, n_qt, num_items;
     int n_k;                 // key rows (K, V); n is the query rows (Q, O)
     const int32_t *pos0;     // chunked prefill: chunk start per sequence, or null
+    // residue classes (dilated and strided patterns; R = 1 otherwise): class c
+    // holds n_hi rows if c < rem, else n_lo; the last q-tile level holds
+    // R_top classes (those with a row in it)
+    int R, rem, n_hi, n_lo, R_top;
+    int rl;                  // landmark stride, 0 for none
     float sl2;  // scale * log2(e)
     __nv_bfloat16 *O;
     float *lse;
@@ -94,30 +99,91 @@ struct PrefillParams {
     int *status;
 };
 
-__device__ __forceinline__ void decode_item(int t, const PrefillParams &p, int &b, int &h, int &kvh,
-                                            int &qt)
+// Work order of both kernels.  Items are ranked by q tile, the last q tile
+// (the most key tiles) first; within a q tile by unit (query head, or head
+// pair), residue class, kv head and sequence, the unit fastest, so the CTAs
+// working at the same time share one band position of every kv head (a few
+// MB of K/V in L2) and, with residue classes, neighbouring rows of it.  Only
+// the last level can hold fewer classes (R_top): a class whose subsequence is
+// one row shorter may end a tile earlier.  No item is empty.
+template <bool PAT>
+__device__ __forceinline__ void decode_level_item(int r, const PrefillParams &p, int U, int &b,
+                                                  int &u, int &kvh, int &qt, int &cls)
 {
-    const int hg = t % p.G;
-    t /= p.G;
-    qt = t % p.n_qt;
-    t /= p.n_qt;
-    kvh = t % p.Hkv;
-    b = t / p.Hkv;
-    h = kvh * p.G + hg;
+    const int per_c = p.B * p.Hkv * U;
+    if constexpr (!PAT) {  // one class: levels of per_c items
+        qt = p.n_qt - 1 - r / per_c;
+        r %= per_c;
+        u = r % U;
+        r /= U;
+        cls = 0;
+        kvh = r % p.Hkv;
+        b = r / p.Hkv;
+        return;
+    }
+    const int top = p.R_top * per_c;
+    int Rl = p.R_top;
+    if (r < top) {
+        qt = p.n_qt - 1;
+    } else {
+        r -= top;
+        const int per_qt = p.R * per_c;
+        qt = p.n_qt - 2 - r / per_qt;
+        r %= per_qt;
+        Rl = p.R;
+    }
+    u = r % U;
+    r /= U;
+    cls = r % Rl;
+    r /= Rl;
+    kvh = r % p.Hkv;
+    b = r / p.Hkv;
 }
 
-// Key tiles of query tile qt of sequence b, in key-list indices; *off is the
-// list index of query row 0 (0 for a plain prefill, chunk_offset(pos0[b]) for
-// a chunked one).
-__device__ __forceinline__ TileRange item_tiles(const PrefillParams &p, int b, int qt, int &off)
+// Key tiles of query tile qt of sequence b (residue class cls), in key-list
+// indices; *off is the list index of query row 0 (0 for a plain prefill,
+// chunk_offset(pos0[b]) for a chunked one).  With residue classes, rows and
+// keys are indices into the class's subsequence.
+template <bool PAT>
+__device__ __forceinline__ TileRange item_tiles(const PrefillParams &p, int b, int qt, int cls,
+                                                int &off)
 {
     off = 0;
     if (p.pos0 != nullptr) {
         const int ps = __ldg(p.pos0 + b);
         off = chunk_offset(ps < 0 ? 0 : ps, p.w, p.g);
     }
-    const int q0 = qt * BM, q1 = (q0 + BM < p.n ? q0 + BM : p.n) - 1;
-    return tile_range_at(q0 + off, q1 + off, p.w, p.g, BN);
+    const int nq = !PAT ? p.n : cls < p.rem ? p.n_hi : p.n_lo;
+    const int q0 = qt * BM, q1 = (q0 + BM < nq ? q0 + BM : nq) - 1;
+    TileRange tr = tile_range_at(q0 + off, q1 + off, p.w, p.g, BN);
+    if constexpr (PAT) add_landmarks(tr, p.w, p.g, p.rl, BN);
+    return tr;
+}
+
+// Key-tile j of an item: its first row in the key source, which view to load
+// it from (landmark tiles: the stride-rl view at class 0), and the element
+// mask a row i applies to it: key index k allowed iff k <= hi and (k >= lo or
+// k < gs), hi/lo/gs per tile kind.
+struct KeyTile {
+    int k0;
+    bool land;
+    bool full;
+};
+template <bool PAT>
+__device__ __forceinline__ KeyTile key_tile(const TileRange &tr, int j, const PrefillParams &p)
+{
+    KeyTile kt;
+    kt.land = PAT && j < tr.nl;
+    if (kt.land) {
+        const int lt = tr.lt0 + j;
+        kt.k0 = lt * BN;
+        kt.full = land_full(tr, lt, p.w, p.g, p.rl, BN);
+    } else {
+        const int t = tile_kt(tr, PAT ? j - tr.nl : j);
+        kt.k0 = t * BN;
+        kt.full = tile_full(tr, t, p.w, p.g, BN);
+    }
+    return kt;
 }
 
 __device__ __forceinline__ float ex2(float x)
@@ -135,11 +201,26 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int HD>
+// One box of rows: with the fixed patterns through the 4-D views (class
+// coordinate cls), otherwise through the plain 3-D maps.
+template <bool PAT>
+__device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x,
+                                          int cls, int row, int z)
+{
+    if constexpr (PAT)
+        tma_load_4d(dst, map, bar, x, cls, row, z);
+    else
+        tma_load_3d(dst, map, bar, x, row, z);
+}
+
+template <int HD, bool PAT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     swa_prefill_bf16_sm103(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK,
-                           const __grid_constant__ CUtensorMap tmV, const PrefillParams p)
+                           const __grid_constant__ CUtensorMap tmV,
+                           const __grid_constant__ CUtensorMap tmQ2,
+                           const __grid_constant__ CUtensorMap tmK2,
+                           const __grid_constant__ CUtensorMap tmV2, const PrefillParams p)
 {
     using L = Layout<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -176,6 +257,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch(&tmQ);
         tma_prefetch(&tmK);
         tma_prefetch(&tmV);
+        tma_prefetch(&tmQ2);
+        tma_prefetch(&tmK2);
+        tma_prefetch(&tmV2);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -195,25 +279,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             last_q_par[0] = last_q_par[1] = -1;
             bool ok = true;
             auto load_q = [&](int item, int idx) -> bool {
-                int b, h, kvh, qt;
-                decode_item(item, p, b, h, kvh, qt);
+                int b, hg, kvh, qt, cls;
+                decode_level_item<PAT>(item, p, p.G, b, hg, kvh, qt, cls);
+                const int h = kvh * p.G + hg;
                 const int qb = idx & 1;
                 if (!mbar_wait(BAR(L::Q_EMPTY + qb), ((idx >> 1) & 1) ^ 1, abort_flag, p.status,
                                TIMEOUT_NS))
                     return false;
                 mbar_expect_tx(BAR(L::Q_FULL + qb), L::QB);
+                const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
                 for (int c = 0; c < HD / 64; ++c)
-                    tma_load_3d(sQ + qb * L::QB + c * (BM * 128), &tmQ, BAR(L::Q_FULL + qb), c * 64,
-                                qt * BM, b * p.H + h);
+                    load_rows<PAT>(sQ + qb * L::QB + c * (BM * 128), mq, BAR(L::Q_FULL + qb),
+                                   c * 64, cls, qt * BM, b * p.H + h);
                 last_q_par[qb] = (idx >> 1) & 1;
                 return true;
             };
             if (static_cast<int>(blockIdx.x) < p.num_items) ok = load_q(blockIdx.x, 0);
             for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
-                int b, h, kvh, qt;
-                decode_item(t, p, b, h, kvh, qt);
+                int b, hg, kvh, qt, cls;
+                decode_level_item<PAT>(t, p, p.G, b, hg, kvh, qt, cls);
                 int off;
-                const TileRange tr = item_tiles(p, b, qt, off);
+                const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
                 for (int j = 0; j < tr.count; ++j, ++kv_iter) {
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
@@ -222,16 +308,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         ok = false;
                         break;
                     }
-                    const int k0 = tile_kt(tr, j) * BN;
+                    const KeyTile kt = key_tile<PAT>(tr, j, p);
                     const int zkv = b * p.Hkv + kvh;
+                    // landmark tiles: class 0 of the stride-rl view; others: this class
+                    const int kc = kt.land ? 0 : cls;
+                    const bool hi = !PAT || kt.land || cls < p.rem;
                     mbar_expect_tx(BAR(L::K_FULL + st), L::KB);
                     for (int c = 0; c < HD / 64; ++c)
-                        tma_load_3d(sK + st * L::KB + c * (BN * 128), &tmK, BAR(L::K_FULL + st),
-                                    c * 64, k0, zkv);
+                        load_rows<PAT>(sK + st * L::KB + c * (BN * 128), hi ? &tmK : &tmK2,
+                                    BAR(L::K_FULL + st), c * 64, kc, kt.k0, zkv);
                     mbar_expect_tx(BAR(L::V_FULL + st), L::KB);
                     for (int c = 0; c < HD / 64; ++c)
-                        tma_load_3d(sV + st * L::KB + c * (BN * 128), &tmV, BAR(L::V_FULL + st),
-                                    c * 64, k0, zkv);
+                        load_rows<PAT>(sV + st * L::KB + c * (BN * 128), hi ? &tmV : &tmV2,
+                                    BAR(L::V_FULL + st), c * 64, kc, kt.k0, zkv);
                     last_k_par[st] = static_cast<int>(ph);
                     if (j == 0 && t + static_cast<int>(gridDim.x) < p.num_items) {
                         // prefetch the next item's Q one item ahead
@@ -291,10 +380,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 return true;
             };
             for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
-                int b, h, kvh, qt;
-                decode_item(t, p, b, h, kvh, qt);
+                int b, hg, kvh, qt, cls;
+                decode_level_item<PAT>(t, p, p.G, b, hg, kvh, qt, cls);
                 int off;
-                const TileRange tr = item_tiles(p, b, qt, off);
+                const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
                 const int qb = it & 1;
                 if (!warp_wait(BAR(L::Q_FULL + qb), (it >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
@@ -348,12 +437,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int c = 0, it = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
-            int b, h, kvh, qt;
-            decode_item(t, p, b, h, kvh, qt);
+            int b, hg, kvh, qt, cls;
+            decode_level_item<PAT>(t, p, p.G, b, hg, kvh, qt, cls);
+            const int h = kvh * p.G + hg;
             int off;
-            const TileRange tr = item_tiles(p, b, qt, off);
+            const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
             const int i = tr.q0 + r;
             const int lo = i - p.w + 1;
+            const int lhi = PAT ? land_hi(i, p.w, p.rl > 0 ? p.rl : 1) : 0;
+            const int llo = PAT && p.rl > 0 ? land_lo(p.g, p.rl) : 0;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < tr.count; ++j, ++c) {
                 const int sbuf = c & 1;
@@ -373,15 +465,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(L::S_EMPTY + sbuf));
 
-                const int kt = tile_kt(tr, j);
-                const int k0 = kt * BN;
-                if (!tile_full(tr, kt, p.w, p.g, BN)) {
+                const KeyTile kt = key_tile<PAT>(tr, j, p);
+                if (!kt.full) {
+                    // band and sink tiles: k <= i and (k >= i-w+1 or k < g); landmark
+                    // tiles (k a landmark index): land_lo <= k <= land_hi(i)
+                    const int khi = kt.land ? lhi : i, klo = kt.land ? llo : lo;
+                    const int kgs = kt.land ? 0 : p.g;
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
-                            const int jj = k0 + q * 32 + e;
-                            const bool allowed = (jj <= i) && (jj >= lo || jj < p.g);
+                            const int jj = kt.k0 + q * 32 + e;
+                            const bool allowed = (jj <= khi) && (jj >= klo || jj < kgs);
                             if (!allowed) s[q][e] = __float_as_uint(-INFINITY);
                         }
                 }
@@ -469,8 +564,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_after();
             float row_lse;
             const float inv_l = finish_row(m, l, p.sink, h, &row_lse);
-            const int t_row = i - off;  // the query row of this thread
-            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + t_row) * HD;
+            // the query row of this thread: its index in the class subsequence,
+            // and its position c + R t
+            const int t_row = i - off;
+            const bool row_ok = t_row < (!PAT ? p.n : cls < p.rem ? p.n_hi : p.n_lo);
+            const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n +
+                                  (PAT ? cls + static_cast<size_t>(p.R) * t_row : t_row);
+            __nv_bfloat16 *orow = p.O + orow_i * HD;
 #pragma unroll 1
             for (int q = 0; q < HD / 32; ++q) {
                 uint32_t o[32];
@@ -482,7 +582,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int e = 0; e < 16; ++e)
                     pkd[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
                                          __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (t_row < p.n) {
+                if (row_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
@@ -492,8 +592,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY));
-            if (p.lse != nullptr && t_row < p.n)
-                p.lse[static_cast<size_t>(b * p.H + h) * p.n + t_row] = row_lse;
+            if (p.lse != nullptr && row_ok) p.lse[orow_i] = row_lse;
         }
     }
 #undef BAR
@@ -569,20 +668,6 @@ __device__ __forceinline__ int pair_item_rank(int c, int k)
     return k * P + ((k & 1) ? P - 1 - c : c);
 }
 
-__device__ __forceinline__ void decode_pair_item(int r, const PrefillParams &p, int &b, int &h0,
-                                                 int &kvh, int &qt)
-{
-    const int pairs = p.G >> 1;
-    const int per_qt = p.B * p.Hkv * pairs;
-    qt = p.n_qt - 1 - r / per_qt;
-    r %= per_qt;
-    const int hp = r % pairs;
-    r /= pairs;
-    kvh = r % p.Hkv;
-    b = r / p.Hkv;
-    h0 = kvh * p.G + 2 * hp;
-}
-
 // Softmax warpgroup x: P_x of the current key tile is in tensor memory.
 __device__ __forceinline__ void p_arrive(int x)
 {
@@ -640,11 +725,14 @@ __device__ __forceinline__ void softmax_half(const uint32_t (&sa)[32], const uin
     }
 }
 
-template <int HD>
+template <int HD, bool PAT>
 __global__ void __launch_bounds__(NTHREADS2, 1)
     swa_prefill_bf16_pair_sm103(const __grid_constant__ CUtensorMap tmQ,
                                 const __grid_constant__ CUtensorMap tmK,
-                                const __grid_constant__ CUtensorMap tmV, const PrefillParams p)
+                                const __grid_constant__ CUtensorMap tmV,
+                                const __grid_constant__ CUtensorMap tmQ2,
+                                const __grid_constant__ CUtensorMap tmK2,
+                                const __grid_constant__ CUtensorMap tmV2, const PrefillParams p)
 {
     using L = Layout2<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -681,6 +769,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         tma_prefetch(&tmQ);
         tma_prefetch(&tmK);
         tma_prefetch(&tmV);
+        tma_prefetch(&tmQ2);
+        tma_prefetch(&tmK2);
+        tma_prefetch(&tmV2);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -702,10 +793,12 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             bool ok = true;
             for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
                  t = pair_item_rank(blockIdx.x, ++it)) {
-                int b, h0, kvh, qt;
-                decode_pair_item(t, p, b, h0, kvh, qt);
+                int b, hp, kvh, qt, cls;
+                decode_level_item<PAT>(t, p, p.G >> 1, b, hp, kvh, qt, cls);
+                const int h0 = kvh * p.G + 2 * hp;
                 int off;
-                const TileRange tr = item_tiles(p, b, qt, off);
+                const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
+                const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
                 for (int x = 0; x < 2 && ok; ++x) {
                     if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
                                    TIMEOUT_NS)) {
@@ -714,8 +807,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     }
                     mbar_expect_tx(BAR(L::Q_FULL + x), L::QB);
                     for (int c = 0; c < HD / 64; ++c)
-                        tma_load_3d(sQ + x * L::QB + c * (BM * 128), &tmQ, BAR(L::Q_FULL + x),
-                                    c * 64, qt * BM, b * p.H + h0 + x);
+                        load_rows<PAT>(sQ + x * L::QB + c * (BM * 128), mq, BAR(L::Q_FULL + x),
+                                       c * 64, cls, qt * BM, b * p.H + h0 + x);
                     last_q_par[x] = it & 1;
                 }
                 for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
@@ -726,17 +819,20 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         ok = false;
                         break;
                     }
-                    const int k0 = tile_kt(tr, j) * BN;
+                    const KeyTile kt = key_tile<PAT>(tr, j, p);
                     const int zkv = b * p.Hkv + kvh;
+                    // landmark tiles: class 0 of the stride-rl view; others: this class
+                    const int kc = kt.land ? 0 : cls;
+                    const bool hi = !PAT || kt.land || cls < p.rem;
                     // K and V of a stage complete one barrier: the MMA issuer waits
                     // once per key tile
                     mbar_expect_tx(BAR(L::K_FULL + st), 2 * L::KB);
                     for (int c = 0; c < HD / 64; ++c)
-                        tma_load_3d(sK + st * L::KB + c * (BN * 128), &tmK, BAR(L::K_FULL + st),
-                                    c * 64, k0, zkv);
+                        load_rows<PAT>(sK + st * L::KB + c * (BN * 128), hi ? &tmK : &tmK2,
+                                    BAR(L::K_FULL + st), c * 64, kc, kt.k0, zkv);
                     for (int c = 0; c < HD / 64; ++c)
-                        tma_load_3d(sV + st * L::KB + c * (BN * 128), &tmV, BAR(L::K_FULL + st),
-                                    c * 64, k0, zkv);
+                        load_rows<PAT>(sV + st * L::KB + c * (BN * 128), hi ? &tmV : &tmV2,
+                                    BAR(L::K_FULL + st), c * 64, kc, kt.k0, zkv);
                     last_k_par[st] = static_cast<int>(ph);
                 }
             }
@@ -808,10 +904,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             using X1 = std::integral_constant<int, 1>;
             for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
                  t = pair_item_rank(blockIdx.x, ++it)) {
-                int b, h0, kvh, qt;
-                decode_pair_item(t, p, b, h0, kvh, qt);
+                int b, hp, kvh, qt, cls;
+                decode_level_item<PAT>(t, p, p.G >> 1, b, hp, kvh, qt, cls);
                 int off;
-                const TileRange tr = item_tiles(p, b, qt, off);
+                const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
                 for (int j = 0; j < tr.count; ++j, ++kv_iter, ++c) {
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
@@ -870,13 +966,15 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         bool ok = true;
         for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
                  t = pair_item_rank(blockIdx.x, ++it)) {
-            int b, h0, kvh, qt;
-            decode_pair_item(t, p, b, h0, kvh, qt);
-            const int h = h0 + x;
+            int b, hp, kvh, qt, cls;
+            decode_level_item<PAT>(t, p, p.G >> 1, b, hp, kvh, qt, cls);
+            const int h = kvh * p.G + 2 * hp + x;
             int off;
-            const TileRange tr = item_tiles(p, b, qt, off);
+            const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
             const int i = tr.q0 + r;
             const int lo = i - p.w + 1;
+            const int lhi = PAT ? land_hi(i, p.w, p.rl > 0 ? p.rl : 1) : 0;
+            const int llo = PAT && p.rl > 0 ? land_lo(p.g, p.rl) : 0;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < tr.count; ++j, ++c) {
                 if (!warp_wait(BAR(L::S_FULL + x), c & 1, abort_flag, p.status)) {
@@ -890,15 +988,18 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < 4; ++q) reg_fence32(s[q]);
-                const int kt = tile_kt(tr, j);
-                const int k0 = kt * BN;
-                if (!tile_full(tr, kt, p.w, p.g, BN)) {
+                const KeyTile kt = key_tile<PAT>(tr, j, p);
+                if (!kt.full) {
+                    // band and sink tiles: k <= i and (k >= i-w+1 or k < g); landmark
+                    // tiles (k a landmark index): land_lo <= k <= land_hi(i)
+                    const int khi = kt.land ? lhi : i, klo = kt.land ? llo : lo;
+                    const int kgs = kt.land ? 0 : p.g;
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
-                            const int jj = k0 + q * 32 + e;
-                            const bool allowed = (jj <= i) && (jj >= lo || jj < p.g);
+                            const int jj = kt.k0 + q * 32 + e;
+                            const bool allowed = (jj <= khi) && (jj >= klo || jj < kgs);
                             if (!allowed) s[q][e] = __float_as_uint(-INFINITY);
                         }
                 }
@@ -959,8 +1060,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             tc_fence_after();
             float row_lse;
             const float inv_l = finish_row(m, l, p.sink, h, &row_lse);
-            const int t_row = i - off;  // the query row of this thread
-            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(b * p.H + h) * p.n + t_row) * HD;
+            // the query row of this thread: its index in the class subsequence,
+            // and its position c + R t
+            const int t_row = i - off;
+            const bool row_ok = t_row < (!PAT ? p.n : cls < p.rem ? p.n_hi : p.n_lo);
+            const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n +
+                                  (PAT ? cls + static_cast<size_t>(p.R) * t_row : t_row);
+            __nv_bfloat16 *orow = p.O + orow_i * HD;
 #pragma unroll 1
             for (int q = 0; q < HD / 32; ++q) {
                 uint32_t o[32];
@@ -972,7 +1078,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 for (int e = 0; e < 16; ++e)
                     pkd[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
                                          __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (t_row < p.n) {
+                if (row_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
@@ -982,8 +1088,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY + x));
-            if (p.lse != nullptr && t_row < p.n)
-                p.lse[static_cast<size_t>(b * p.H + h) * p.n + t_row] = row_lse;
+            if (p.lse != nullptr && row_ok) p.lse[orow_i] = row_lse;
         }
         // gave up (a wait ran out): one more arrival lets an issuer that is
         // already waiting for this head's P meet, see the abort flag and stop
@@ -1136,24 +1241,107 @@ bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 4-D view of a bf16 tensor [Z][rows_total][d]: dims (d, R, rows, Z), byte
+// strides (d*2, R*d*2, rows_total*d*2), so element (x, c, k, z) is column x of
+// row c + R*k of slice z, and a box (64, 1, box_rows, 1) taken at class c is
+// box_rows rows R apart.  R = 1 is the plain row-major tensor.  The caller
+// keeps c + R*(rows-1) < rows_total for every class a box is taken at, so no
+// box reaches past its slice.
+bool make_view(CUtensorMap *m, const void *base, uint64_t d, uint64_t R, uint64_t rows,
+               uint64_t Z, uint64_t rows_total, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[4] = {d, R, rows, Z};
+    cuuint64_t strides[3] = {d * 2, R * d * 2, rows_total * d * 2};
+    cuuint32_t box[4] = {64, 1, box_rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Opt in to a kernel's dynamic shared memory once (one flag per kernel: the
+// kernel itself is the template argument).
+template <auto Kernel>
+cudaError_t set_smem_once(uint32_t bytes)
+{
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [&] {
+        err = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
+    return err;
+}
+
+template <int HD, bool PAT>
+int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                   const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
+                   PrefillParams p, int per_unit, cudaStream_t stream)
+{
+    if (p.G % 2 == 0 && std::getenv("SWA_PREFILL_SINGLE") == nullptr) {
+        // two heads of a GQA pair per work item
+        using L2 = Layout2<HD>;
+        if (set_smem_once<swa_prefill_bf16_pair_sm103<HD, PAT>>(L2::DYN_SMEM) != cudaSuccess)
+            return SWA_ERR_CUDA;
+        p.num_items = p.B * p.Hkv * (p.G / 2) * per_unit;
+        const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
+        swa_prefill_bf16_pair_sm103<HD, PAT>
+            <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
+        return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+    }
+    using L = Layout<HD>;
+    if (set_smem_once<swa_prefill_bf16_sm103<HD, PAT>>(L::DYN_SMEM) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    p.num_items = p.B * p.H * per_unit;
+    const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
+    swa_prefill_bf16_sm103<HD, PAT>
+        <<<grid, NTHREADS, L::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
+    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
 template <int HD>
 int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, const float *sink,
               int B, int H, int Hkv, int n, int n_k, int w, int g, float scale,
-              const int32_t *pos0, cudaStream_t stream)
+              const int32_t *pos0, int R, int rl, cudaStream_t stream)
 {
-    using L = Layout<HD>;
-    CUtensorMap mq, mk, mv;
-    if (!make_map_3d(&mq, Q, HD, n, static_cast<uint64_t>(B) * H, BM) ||
-        !make_map_3d(&mk, K, HD, n_k, static_cast<uint64_t>(B) * Hkv, BN) ||
-        !make_map_3d(&mv, V, HD, n_k, static_cast<uint64_t>(B) * Hkv, BN))
-        return SWA_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(swa_prefill_bf16_sm103<HD>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
-    });
-    if (attr_err != cudaSuccess) return SWA_ERR_CUDA;
+    if (rl > 0) R = 1;
+    const bool pat = R > 1 || rl > 0;
+    // residue classes: class c has n_hi rows if c < rem, else n_lo
+    const int n_hi = (n + R - 1) / R, n_lo = n / R, rem = n % R;
+    const uint64_t ZQ = static_cast<uint64_t>(B) * H, ZK = static_cast<uint64_t>(B) * Hkv;
+    // maps: tmX for classes below rem (and the landmark view), tmX2 for the rest
+    CUtensorMap mq, mk, mv, mq2, mk2, mv2;
+    bool ok;
+    if (!pat) {
+        ok = make_map_3d(&mq, Q, HD, n, ZQ, BM) && make_map_3d(&mk, K, HD, n_k, ZK, BN) &&
+             make_map_3d(&mv, V, HD, n_k, ZK, BN);
+        mq2 = mq;
+        mk2 = mk;
+        mv2 = mv;
+    } else if (rl > 0) {
+        // landmarks: Q, K, V as they are, and K, V as the stride-rl view whose
+        // class 0 lists positions 0, rl, 2 rl, ... (ceil(n/rl) of them)
+        const uint64_t nlm = (static_cast<uint64_t>(n_k) + rl - 1) / rl;
+        ok = make_view(&mq2, Q, HD, 1, n, ZQ, n, BM) && make_view(&mk2, K, HD, 1, n_k, ZK, n_k, BN) &&
+             make_view(&mv2, V, HD, 1, n_k, ZK, n_k, BN) &&
+             make_view(&mk, K, HD, rl, nlm, ZK, n_k, BN) && make_view(&mv, V, HD, rl, nlm, ZK, n_k, BN);
+        mq = mq2;
+    } else {
+        ok = make_view(&mq, Q, HD, R, n_hi, ZQ, n, BM) &&
+             make_view(&mk, K, HD, R, n_hi, ZK, n_k, BN) &&
+             make_view(&mv, V, HD, R, n_hi, ZK, n_k, BN);
+        if (ok && n_lo > 0 && n_lo != n_hi) {
+            ok = make_view(&mq2, Q, HD, R, n_lo, ZQ, n, BM) &&
+                 make_view(&mk2, K, HD, R, n_lo, ZK, n_k, BN) &&
+                 make_view(&mv2, V, HD, R, n_lo, ZK, n_k, BN);
+        } else {
+            mq2 = mq;
+            mk2 = mk;
+            mv2 = mv;
+        }
+    }
+    if (!ok) return SWA_ERR_CUDA;
     PrefillParams p;
     p.B = B;
     p.H = H;
@@ -1164,45 +1352,39 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     p.w = w;
     p.g = g;
     p.G = H / Hkv;
-    p.n_qt = (n + BM - 1) / BM;
-    p.num_items = B * H * p.n_qt;
+    p.R = R;
+    p.rem = rem;
+    p.n_hi = n_hi;
+    p.n_lo = n_lo;
+    p.rl = rl;
+    p.n_qt = (n_hi + BM - 1) / BM;
+    p.R_top = n_lo > (p.n_qt - 1) * BM ? R : rem;
+    p.num_items = 0;
+    // items per unit (query head or head pair) of one kv head of one sequence
+    const int per_unit = p.R_top + (p.n_qt - 1) * R;
     p.sl2 = scale * 1.4426950408889634f;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.lse = lse;
     p.sink = sink;
     p.status = status_ptr();
     if (p.status == nullptr) return SWA_ERR_CUDA;
-    if (p.G % 2 == 0 && std::getenv("SWA_PREFILL_SINGLE") == nullptr) {
-        // two heads of a GQA pair per work item
-        using L2 = Layout2<HD>;
-        static std::once_flag attr2_once;
-        static cudaError_t attr2_err = cudaSuccess;
-        std::call_once(attr2_once, [] {
-            attr2_err = cudaFuncSetAttribute(swa_prefill_bf16_pair_sm103<HD>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             L2::DYN_SMEM);
-        });
-        if (attr2_err != cudaSuccess) return SWA_ERR_CUDA;
-        p.num_items = B * Hkv * p.n_qt * (p.G / 2);
-        const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-        swa_prefill_bf16_pair_sm103<HD><<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, p);
-        return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
-    }
-    const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-    swa_prefill_bf16_sm103<HD><<<grid, NTHREADS, L::DYN_SMEM, stream>>>(mq, mk, mv, p);
-    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+    if (pat) return launch_kernels<HD, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream);
+    return launch_kernels<HD, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream);
 }
 
 }  // namespace
 
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
                         const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
-                        int g, float scale, const int32_t *pos0, cudaStream_t stream)
+                        int g, float scale, const int32_t *pos0, int R, int rl,
+                        cudaStream_t stream)
 {
     if (d == 128)
-        return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, stream);
+        return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
+                              stream);
     if (d == 64)
-        return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, stream);
+        return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
+                             stream);
     return SWA_ERR_UNSUPPORTED;
 }
 
