@@ -45,6 +45,13 @@ PREFILL_WORKLOADS = {
     # the full-causal global layer of the Gemma-3 hybrid (w >= n)
     "gemma3_global_prefill": dict(B=2, H=32, Hkv=16, n=32768, d=128, w=32768, g=0,
                                   sink_scale=1.0),
+    # other fixed patterns (swa_prefill_pattern)
+    "dilated_prefill": dict(B=1, H=32, Hkv=8, n=16384, d=128, w=1024, g=0, sink_scale=1.0,
+                            pattern="dilated", r=4),
+    "strided_prefill": dict(B=1, H=32, Hkv=8, n=65536, d=128, w=0, g=0, sink_scale=1.0,
+                            pattern="strided", r=256),
+    "landmark_prefill": dict(B=1, H=32, Hkv=8, n=16384, d=128, w=4096, g=4, sink_scale=4.0,
+                             pattern="landmark", r=64),
 }
 PREFILL = PREFILL_WORKLOADS["mistral_like_prefill"]
 # a prompt chunk of T tokens at position pos0 against a full rolling cache
@@ -65,8 +72,29 @@ def pairs(n, w, g):
     return total
 
 
+def row_keys(i, c):
+    """Keys query position i reads under workload c's pattern (i: int or array).
+    window: the band and the sinks; dilated: i, i-r, ..., i-(w-1)r; strided:
+    every (i-j) mod r == 0; landmark: the band, the sinks and the positions
+    j mod r == 0 before the band that are not sinks."""
+    i = np.asarray(i, dtype=np.int64)
+    w, g = c["w"], c["g"]
+    pat, r = c.get("pattern", "window"), c.get("r", 1)
+    if pat == "dilated":
+        return np.minimum(w, i // r + 1)
+    if pat == "strided":
+        return i // r + 1
+    keys = np.minimum(i + 1, w) + np.minimum(g, np.maximum(0, i - w + 1))
+    if pat == "landmark":
+        lm = np.where(i >= w, (i - w) // r - (g + r - 1) // r + 1, 0)
+        keys = keys + np.maximum(0, lm)
+    return keys
+
+
 def prefill_flops(c):
-    return 4 * pairs(c["n"], c["w"], c["g"]) * c["d"] * c["B"] * c["H"]
+    if c.get("pattern", "window") == "window":
+        return 4 * pairs(c["n"], c["w"], c["g"]) * c["d"] * c["B"] * c["H"]
+    return 4 * int(row_keys(np.arange(c["n"]), c).sum()) * c["d"] * c["B"] * c["H"]
 
 
 def chunk_flops(c):
@@ -226,11 +254,13 @@ def cpu_oracle_sample(min_seconds=10.0, max_seconds=30.0, seed=0, c=None):
         rows = rows_all[done:done + batch]
         qr = np.stack([x.Q[b, h, i].double().numpy() for b, h, i in rows])
         t0 = time.perf_counter()
-        oracle.prefill_rows(qr, K, V, c["H"], c["w"], c["g"], x.scale, rows)
+        if c.get("pattern", "window") == "window":
+            oracle.prefill_rows(qr, K, V, c["H"], c["w"], c["g"], x.scale, rows)
+        else:
+            oracle.prefill_pattern_rows(qr, K, V, c["H"], c["w"], c["g"], c["r"], c["pattern"],
+                                        x.scale, rows)
         t_total += time.perf_counter() - t0
-        for _, _, i in rows:
-            i = int(i)
-            flops += 4 * c["d"] * (min(i + 1, c["w"]) + min(c["g"], max(0, i - c["w"] + 1)))
+        flops += 4 * c["d"] * int(row_keys(rows[:, 2], c).sum())
         done += rows.shape[0]
         if t_total < min_seconds / 4:
             batch *= 2
@@ -292,7 +322,13 @@ def run_swa(args):
                                      dtype="bf16", seed=rank, sink_scale=c["sink_scale"],
                                      device=dev)
         out = torch.empty_like(x.Q)
-        fn = lambda: swa.prefill(x.Q, x.K, x.V, c["w"], c["g"], x.scale, out=out, stream=stream)
+        if c.get("pattern", "window") == "window":
+            call = lambda Q, K, V: swa.prefill(Q, K, V, c["w"], c["g"], x.scale, out=out,
+                                               stream=stream)
+        else:
+            call = lambda Q, K, V: swa.prefill_pattern(Q, K, V, c["pattern"], c["w"], c["g"],
+                                                       c["r"], x.scale, out=out, stream=stream)
+        fn = lambda: call(x.Q, x.K, x.V)
         barrier(world)
         torch.cuda.synchronize()
         with Clocks(local) as clk:
@@ -319,7 +355,7 @@ def run_swa(args):
                 Qd.copy_(Qh, non_blocking=True)
                 Kd.copy_(Kh, non_blocking=True)
                 Vd.copy_(Vh, non_blocking=True)
-                swa.prefill(Qd, Kd, Vd, c["w"], c["g"], x.scale, out=out, stream=stream)
+                call(Qd, Kd, Vd)
                 Oh.copy_(out, non_blocking=True)
 
             e2e_times = time_launches(e2e_step, max(2, args.steps // 2), 2, flush, stream)

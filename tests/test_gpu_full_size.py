@@ -8,6 +8,9 @@ Workloads (inputs seeded exactly as the benchmark seeds them):
   gemma3_local_prefill   B=2 H=32 Hkv=16 n=32768  d=128 w=1024 g=0
   long_sink_prefill      B=1 H=32 Hkv=8  n=131072 d=128 w=4096 g=4, sink keys x4
   gemma3_global_prefill  B=2 H=32 Hkv=16 n=32768  d=128 w=n (full causal) g=0
+  dilated_prefill        B=1 H=32 Hkv=8  n=16384  d=128 dilated w=1024 r=4
+  strided_prefill        B=1 H=32 Hkv=8  n=65536  d=128 strided r=256
+  landmark_prefill       B=1 H=32 Hkv=8  n=16384  d=128 w=4096 g=4 landmarks r=64
 """
 import numpy as np
 import pytest
@@ -21,21 +24,26 @@ N_SAMPLED = 64
 
 def edge_rows(B, H, n, w, g):
     cand = {0, 1, 3, g, w - 2, w - 1, w, w + 1, w + g - 1, w + g, w + g + 1, 4095, 4096, 4098,
-            4099, n // 2, n - 2, n - 1}
+            4099, 255, 256, 257, 1023, 1024, n // 2, n - 2, n - 1}
     rows = sorted(i for i in cand if 0 <= i < n)
     return [(B - 1, h, i) for h in (0, H - 1) for i in rows]
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", ["mistral_like_prefill", "gemma3_local_prefill",
-                                  "long_sink_prefill", "gemma3_global_prefill"])
+                                  "long_sink_prefill", "gemma3_global_prefill",
+                                  "dilated_prefill", "strided_prefill", "landmark_prefill"])
 def test_prefill_full_size_sampled_rows(swa, oracle_mod, name):
     c = synthetic.WORKLOADS[name]
     B, H, Hkv, n, d, w, g = (c[k] for k in ("B", "H", "Hkv", "n", "d", "w", "g"))
+    pattern, r = c.get("pattern", "window"), c.get("r", 1)
     x = synthetic.prefill_inputs(B, H, Hkv, n, d, w, g, dtype="bf16", seed=0,
                                  sink_scale=c["sink_scale"], device="cuda")
     lse = torch.empty(B, H, n, dtype=torch.float32, device="cuda")
-    out = swa.prefill(x.Q, x.K, x.V, w, g, x.scale, lse=lse)
+    if pattern == "window":
+        out = swa.prefill(x.Q, x.K, x.V, w, g, x.scale, lse=lse)
+    else:
+        out = swa.prefill_pattern(x.Q, x.K, x.V, pattern, w, g, r, x.scale, lse=lse)
     torch.cuda.synchronize()
     assert swa.device_status() == 0
     rows = synthetic.sample_rows(B, H, n, N_SAMPLED, seed=1).numpy()
@@ -47,7 +55,11 @@ def test_prefill_full_size_sampled_rows(swa, oracle_mod, name):
     Kh, Vh = x.K.cpu(), x.V.cpu()
     del x, out, lse
     torch.cuda.empty_cache()
-    O, L = oracle_mod.prefill_rows(q_rows, Kh, Vh, H, w, g, synthetic.default_scale(d), rows)
+    if pattern == "window":
+        O, L = oracle_mod.prefill_rows(q_rows, Kh, Vh, H, w, g, synthetic.default_scale(d), rows)
+    else:
+        O, L = oracle_mod.prefill_pattern_rows(q_rows, Kh, Vh, H, w, g, r, pattern,
+                                               synthetic.default_scale(d), rows)
     assert np.isfinite(got).all()
     err = np.abs(got - O)
     assert err.max() <= BF16_MAX_ABS and err.mean() <= BF16_MEAN_ABS, \
