@@ -54,6 +54,14 @@ constexpr uint32_t S_COL0 = 128;
 constexpr uint32_t P_COL0 = 384;
 constexpr float RESCALE_LOG2 = 8.0f;
 
+// Epilogue staging: each softmax warp turns its 32 rows x 32 columns of the
+// output (64 bytes of bf16 per row) around in shared memory so that its global
+// stores cover whole 64-byte row segments, 8 rows per instruction, instead of
+// 16 bytes of 32 different rows.  Rows are padded to 80 bytes, so the 16-byte
+// accesses of 8 lanes in a row fall in distinct banks.
+constexpr uint32_t STAGE_ROW = 80;
+constexpr uint32_t STAGE_WARP = 32 * STAGE_ROW;
+
 template <int HD>
 struct Layout {
     static constexpr uint32_t QB = BM * HD * 2;    // one Q tile
@@ -77,7 +85,8 @@ struct Layout {
         NBAR = DRAIN + 1
     };
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t BYTES = MISC_OFF + 16;
+    static constexpr uint32_t STAGE_OFF = (MISC_OFF + 16 + 15) & ~15u;  // 4 softmax warps
+    static constexpr uint32_t BYTES = STAGE_OFF + 4 * STAGE_WARP;
     // > half of the SM's shared memory, so that exactly one CTA (and one
     // 512-column TMEM allocation) lives on an SM.
     static constexpr uint32_t DYN_SMEM = (BYTES + 1024 > 120 * 1024) ? BYTES + 1024 : 120 * 1024;
@@ -199,6 +208,55 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 {
     const bool ok = mbar_wait(bar, parity, abort, status, TIMEOUT_NS);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Epilogue of one warp: the 32 query rows of its TMEM lane quarter (one per
+// lane), O[:, 0:HD) at o_addr, times inv_l, rounded to bf16 and stored to
+// orow (this lane's output row; row_ok false for rows past the end) through
+// the warp's staging area `stage` (STAGE_WARP bytes of shared memory).
+template <int HD>
+__device__ __forceinline__ void store_o_rows(uint32_t o_addr, float inv_l,
+                                             __nv_bfloat16 *orow, bool row_ok, uint8_t *stage,
+                                             int lane)
+{
+    // the row each lane writes back in step s: 8 rows per step, 4 lanes a row
+    const int sub = lane & 3;
+    uint64_t dst[4];
+    bool dok[4];
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+        const int src = st * 8 + (lane >> 2);
+        dst[st] = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(orow), src);
+        dok[st] = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, src) != 0;
+    }
+    uint4 *mine = reinterpret_cast<uint4 *>(stage + lane * STAGE_ROW);
+#pragma unroll 1
+    for (int q = 0; q < HD / 32; ++q) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + q * 32, o);
+        tmem_ld_wait();
+        reg_fence32(o);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+            mine[v] = make_uint4(
+                pack_bf16x2(__uint_as_float(o[8 * v]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
+                pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l,
+                            __uint_as_float(o[8 * v + 3]) * inv_l),
+                pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l,
+                            __uint_as_float(o[8 * v + 5]) * inv_l),
+                pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l,
+                            __uint_as_float(o[8 * v + 7]) * inv_l));
+        __syncwarp();
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+            const uint4 val =
+                *reinterpret_cast<const uint4 *>(stage + (st * 8 + (lane >> 2)) * STAGE_ROW + sub * 16);
+            if (dok[st])
+                reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(dst[st]) + q * 32)[sub] =
+                    val;
+        }
+        __syncwarp();
+    }
 }
 
 // One box of rows: with the fixed patterns through the 4-D views (class
@@ -571,24 +629,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n +
                                   (PAT ? cls + static_cast<size_t>(p.R) * t_row : t_row);
             __nv_bfloat16 *orow = p.O + orow_i * HD;
-#pragma unroll 1
-            for (int q = 0; q < HD / 32; ++q) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + q * 32, o);
-                tmem_ld_wait();
-                reg_fence32(o);
-                uint32_t pkd[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pkd[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
-                                         __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (row_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
-                }
-            }
+            store_o_rows<HD>(tmem + lane_off, inv_l, orow, row_ok,
+                             smem + L::STAGE_OFF + (warp - 2) * STAGE_WARP, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY));
@@ -651,7 +693,8 @@ struct Layout2 {
         NBAR = DRAIN + 1
     };
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t BYTES = MISC_OFF + 16;
+    static constexpr uint32_t STAGE_OFF = (MISC_OFF + 16 + 15) & ~15u;  // 8 softmax warps
+    static constexpr uint32_t BYTES = STAGE_OFF + 8 * STAGE_WARP;
     static constexpr uint32_t DYN_SMEM = (BYTES + 1024 > 120 * 1024) ? BYTES + 1024 : 120 * 1024;
 };
 
@@ -1067,24 +1110,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n +
                                   (PAT ? cls + static_cast<size_t>(p.R) * t_row : t_row);
             __nv_bfloat16 *orow = p.O + orow_i * HD;
-#pragma unroll 1
-            for (int q = 0; q < HD / 32; ++q) {
-                uint32_t o[32];
-                tmem_ld32(o_addr + q * 32, o);
-                tmem_ld_wait();
-                reg_fence32(o);
-                uint32_t pkd[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pkd[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
-                                         __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (row_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
-                }
-            }
+            store_o_rows<HD>(o_addr, inv_l, orow, row_ok,
+                             smem + L::STAGE_OFF + (warp - 4) * STAGE_WARP, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY + x));
