@@ -529,14 +529,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // tiles (k a landmark index): land_lo <= k <= land_hi(i)
                     const int khi = kt.land ? lhi : i, klo = kt.land ? llo : lo;
                     const int kgs = kt.land ? 0 : p.g;
+                    // in tile columns c = k - k0: allowed iff c <= cb and (c >= ca or
+                    // c < cg); one bound alone decides on nearly every partial tile
+                    const int ca = klo - kt.k0, cb = khi - kt.k0, cg = kgs - kt.k0;
+                    if (cg >= ca || ca <= 0) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                        for (int q = 0; q < 4; ++q)
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int jj = kt.k0 + q * 32 + e;
-                            const bool allowed = (jj <= khi) && (jj >= klo || jj < kgs);
-                            if (!allowed) s[q][e] = __float_as_uint(-INFINITY);
-                        }
+                            for (int e = 0; e < 32; ++e)
+                                if (q * 32 + e > cb) s[q][e] = __float_as_uint(-INFINITY);
+                    } else if (cb >= BN - 1 && cg <= 0) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (q * 32 + e < ca) s[q][e] = __float_as_uint(-INFINITY);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int c = q * 32 + e;
+                                if (!(c <= cb && (c >= ca || c < cg)))
+                                    s[q][e] = __float_as_uint(-INFINITY);
+                            }
+                    }
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -1037,14 +1054,34 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     // tiles (k a landmark index): land_lo <= k <= land_hi(i)
                     const int khi = kt.land ? lhi : i, klo = kt.land ? llo : lo;
                     const int kgs = kt.land ? 0 : p.g;
+                    // in tile columns c = k - k0: allowed iff c <= cb and (c >= ca or
+                    // c < cg).  Nearly always one bound alone decides (the diagonal
+                    // tile: c <= cb; the tile where the band starts: c >= ca), so
+                    // those rows test one bound per element
+                    const int ca = klo - kt.k0, cb = khi - kt.k0, cg = kgs - kt.k0;
+                    if (cg >= ca || ca <= 0) {
+                        // the sinks (if any) reach the band, or the band covers c >= 0
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                        for (int q = 0; q < 4; ++q)
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int jj = kt.k0 + q * 32 + e;
-                            const bool allowed = (jj <= khi) && (jj >= klo || jj < kgs);
-                            if (!allowed) s[q][e] = __float_as_uint(-INFINITY);
-                        }
+                            for (int e = 0; e < 32; ++e)
+                                if (q * 32 + e > cb) s[q][e] = __float_as_uint(-INFINITY);
+                    } else if (cb >= BN - 1 && cg <= 0) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (q * 32 + e < ca) s[q][e] = __float_as_uint(-INFINITY);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int c = q * 32 + e;
+                                if (!(c <= cb && (c >= ca || c < cg)))
+                                    s[q][e] = __float_as_uint(-INFINITY);
+                            }
+                    }
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
