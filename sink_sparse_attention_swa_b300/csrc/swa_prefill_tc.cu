@@ -230,22 +230,25 @@ __device__ __forceinline__ void store_o_rows(uint32_t o_addr, float inv_l,
         dok[st] = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, src) != 0;
     }
     uint4 *mine = reinterpret_cast<uint4 *>(stage + lane * STAGE_ROW);
-#pragma unroll 1
+    // all of the row's O columns in one round of tensor-memory loads
+    uint32_t o[HD / 32][32];
+#pragma unroll
+    for (int q = 0; q < HD / 32; ++q) tmem_ld32(o_addr + q * 32, o[q]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < HD / 32; ++q) reg_fence32(o[q]);
+#pragma unroll
     for (int q = 0; q < HD / 32; ++q) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + q * 32, o);
-        tmem_ld_wait();
-        reg_fence32(o);
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-            mine[v] = make_uint4(
-                pack_bf16x2(__uint_as_float(o[8 * v]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l,
-                            __uint_as_float(o[8 * v + 3]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l,
-                            __uint_as_float(o[8 * v + 5]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l,
-                            __uint_as_float(o[8 * v + 7]) * inv_l));
+            mine[v] = make_uint4(pack_bf16x2(__uint_as_float(o[q][8 * v]) * inv_l,
+                                             __uint_as_float(o[q][8 * v + 1]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(o[q][8 * v + 2]) * inv_l,
+                                             __uint_as_float(o[q][8 * v + 3]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(o[q][8 * v + 4]) * inv_l,
+                                             __uint_as_float(o[q][8 * v + 5]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(o[q][8 * v + 6]) * inv_l,
+                                             __uint_as_float(o[q][8 * v + 7]) * inv_l));
         __syncwarp();
 #pragma unroll
         for (int st = 0; st < 4; ++st) {
@@ -1024,13 +1027,24 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         const uint64_t sl2x2 = pack2(__float_as_uint(sl2), __float_as_uint(sl2));
         int c = 0, it = 0;
         bool ok = true;
-        for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
-                 t = pair_item_rank(blockIdx.x, ++it)) {
-            int b, hp, kvh, qt, cls;
-            decode_level_item<PAT>(t, p, p.G >> 1, b, hp, kvh, qt, cls);
-            const int h = kvh * p.G + 2 * hp + x;
-            int off;
-            const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
+        // the item's sequence, head, class, query offset and key tiles; the next
+        // item's are worked out while this one's last P V runs
+        struct Item {
+            int b, h, cls, off;
+            TileRange tr;
+        };
+        auto load_item = [&](int t, Item &e) {
+            int hp, kvh, qt;
+            decode_level_item<PAT>(t, p, p.G >> 1, e.b, hp, kvh, qt, e.cls);
+            e.h = kvh * p.G + 2 * hp + x;
+            e.tr = item_tiles<PAT>(p, e.b, qt, e.cls, e.off);
+        };
+        Item nxt;
+        int t = pair_item_rank(blockIdx.x, 0);
+        if (t < pairs_per_item_count) load_item(t, nxt);
+        while (ok && t < pairs_per_item_count) {
+            const int b = nxt.b, h = nxt.h, cls = nxt.cls, off = nxt.off;
+            const TileRange tr = nxt.tr;
             const int i = tr.q0 + r;
             const int lo = i - p.w + 1;
             const int lhi = PAT ? land_hi(i, p.w, p.rl > 0 ? p.rl : 1) : 0;
@@ -1133,11 +1147,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
-            if (!warp_wait(BAR(L::O_FULL + x), it & 1, abort_flag, p.status)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
+            // the row's normaliser and output address, and the next item, while
+            // the last P V of this one is still running
             float row_lse;
             const float inv_l = finish_row(m, l, p.sink, h, &row_lse);
             // the query row of this thread: its index in the class subsequence,
@@ -1147,12 +1158,21 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n +
                                   (PAT ? cls + static_cast<size_t>(p.R) * t_row : t_row);
             __nv_bfloat16 *orow = p.O + orow_i * HD;
+            const int t_next = pair_item_rank(blockIdx.x, it + 1);
+            if (t_next < pairs_per_item_count) load_item(t_next, nxt);
+            if (!warp_wait(BAR(L::O_FULL + x), it & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
             store_o_rows<HD>(o_addr, inv_l, orow, row_ok,
                              smem + L::STAGE_OFF + (warp - 4) * STAGE_WARP, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(L::O_EMPTY + x));
             if (p.lse != nullptr && row_ok) p.lse[orow_i] = row_lse;
+            ++it;
+            t = t_next;
         }
         // gave up (a wait ran out): one more arrival lets an issuer that is
         // already waiting for this head's P meet, see the abort flag and stop
