@@ -283,6 +283,21 @@ int64_t swa_count_pairs(int64_t n, int64_t w, int64_t g);
 int swa_enumerate_tiles(int64_t n, int64_t w, int64_t g, int BM, int BN, int32_t *cls,
                         size_t cap);
 
+/*
+ * Landmark tiles of the landmark pattern (swa_prefill_pattern with
+ * SWA_PATTERN_LANDMARK; "Local and Sparse Attention: Reading Fewer Token
+ * Positions", Figure 2, right).  The landmarks 0, r, 2r, ... form a list
+ * indexed by m (position r*m); for query tile qt (rows qt*BM ..) and landmark
+ * tile lt (landmarks lt*BN ..), cls[qt*n_lt + lt] = 0 not visited, 1 partial,
+ * 2 full, n_lt = ceil(ceil(n/r)/BN).  These tiles carry only the landmarks a
+ * row reads outside its band and sinks (g <= r*m <= i-w); the band and sink
+ * tiles are those of swa_enumerate_tiles.  Landmarks past the list count as
+ * blocked.  Host memory, `cap` int32 elements.  Returns SWA_OK or
+ * SWA_ERR_INVALID_ARG.
+ */
+int swa_enumerate_landmark_tiles(int64_t n, int64_t w, int64_t g, int64_t r, int BM, int BN,
+                                 int32_t *cls, size_t cap);
+
 /* Where the rolling cache keeps position p: *ring_slot = p mod w,
  * *sink_slot = w+p if p < g else -1.  Returns SWA_OK or SWA_ERR_INVALID_ARG. */
 int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_slot);

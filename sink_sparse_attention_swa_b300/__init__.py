@@ -22,7 +22,8 @@ import torch
 __all__ = [
     "SwaError", "prefill", "prefill_pattern", "prefill_chunk", "prefill_chunk_workspace_bytes",
     "PATTERNS", "decode", "cache_append", "decode_workspace_bytes",
-    "count_pairs", "enumerate_tiles", "cache_slot", "device_status", "selftest_umma",
+    "count_pairs", "enumerate_tiles", "enumerate_landmark_tiles", "cache_slot", "device_status",
+    "selftest_umma",
     "library_path", "lib",
 ]
 
@@ -54,6 +55,7 @@ SIGNATURES = {
     "swa_cache_append": (_i, [_p, _p, _p, _p, _p] + [_i] * 6 + [_i, _p]),
     "swa_count_pairs": (_i64, [_i64, _i64, _i64]),
     "swa_enumerate_tiles": (_i, [_i64, _i64, _i64, _i, _i, _p, _sz]),
+    "swa_enumerate_landmark_tiles": (_i, [_i64, _i64, _i64, _i64, _i, _i, _p, _sz]),
     "swa_cache_slot": (_i, [_i64, _i, _i, _p, _p]),
     "swa_get_device_status": (_i, [_p]),
     "swa_status_string": (ctypes.c_char_p, [_i]),
@@ -305,6 +307,15 @@ def enumerate_tiles(n: int, w: int, g: int, BM: int, BN: int):
     nq, nk = -(-n // BM), -(-n // BN)
     out = torch.zeros(nq, nk, dtype=torch.int32)
     _check("swa_enumerate_tiles", _load().swa_enumerate_tiles(n, w, g, BM, BN, out.data_ptr(), out.numel()))
+    return out
+
+
+def enumerate_landmark_tiles(n: int, w: int, g: int, r: int, BM: int, BN: int):
+    """Landmark tile classes [ceil(n/BM), ceil(ceil(n/r)/BN)] int32 (0/1/2), host-only."""
+    nq, nk = -(-n // BM), -(-(-(-n // r)) // BN)
+    out = torch.zeros((nq, nk), dtype=torch.int32)
+    rc = _load().swa_enumerate_landmark_tiles(n, w, g, r, BM, BN, out.data_ptr(), out.numel())
+    _check("swa_enumerate_landmark_tiles", rc)
     return out
 
 

@@ -287,6 +287,31 @@ int swa_enumerate_tiles(int64_t n, int64_t w, int64_t g, int BM, int BN, int32_t
     return SWA_OK;
 }
 
+int swa_enumerate_landmark_tiles(int64_t n, int64_t w, int64_t g, int64_t r, int BM, int BN,
+                                 int32_t *cls, size_t cap)
+{
+    if (n < 1 || n > INT32_MAX / 2 || w < 1 || g < 0 || r < 1 || BM < 1 || BN < 1 ||
+        cls == nullptr)
+        return SWA_ERR_INVALID_ARG;
+    const int64_t nl = (n + r - 1) / r;  // landmarks 0, r, 2r, ...
+    const int64_t nq = (n + BM - 1) / BM, nk = (nl + BN - 1) / BN;
+    if (static_cast<uint64_t>(nq) * static_cast<uint64_t>(nk) > cap) return SWA_ERR_INVALID_ARG;
+    const int wi = static_cast<int>(w < INT32_MAX / 2 ? w : INT32_MAX / 2);
+    const int gi = static_cast<int>(g < INT32_MAX / 2 ? g : INT32_MAX / 2);
+    const int ri = static_cast<int>(r < INT32_MAX / 2 ? r : INT32_MAX / 2);
+    std::memset(cls, 0, sizeof(int32_t) * static_cast<size_t>(nq * nk));
+    for (int qt = 0; qt < nq; ++qt) {
+        TileRange tr = tile_range(qt, static_cast<int>(n), wi, gi, BM, BN);
+        tr.count = 0;
+        add_landmarks(tr, wi, gi, ri, BN);
+        for (int j = 0; j < tr.nl; ++j) {
+            const int lt = tr.lt0 + j;
+            cls[static_cast<size_t>(qt) * nk + lt] = land_full(tr, lt, wi, gi, ri, BN) ? 2 : 1;
+        }
+    }
+    return SWA_OK;
+}
+
 int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_slot)
 {
     if (p < 0 || w < 1 || g < 0 || ring_slot == nullptr || sink_slot == nullptr)

@@ -117,3 +117,35 @@ def test_host_validation_rejects_before_launch(swa):
     assert L.swa_cache_append(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 1, 2, 128, 8, 0, 0, None) == -1
     assert L.swa_cache_append(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 1, 1, 2, 128, 8, 0, 0, None) == -1
     assert L.swa_cache_append(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 2, 128, 8, 0, 0, None) == 0
+
+
+@pytest.mark.parametrize("n,w,g,r,BM,BN", [
+    (300, 20, 0, 4, 32, 16), (500, 64, 3, 7, 64, 32), (257, 8, 9, 2, 16, 16),
+    (1000, 100, 1, 50, 128, 128), (90, 200, 2, 5, 32, 8), (400, 30, 40, 8, 32, 32),
+])
+def test_landmark_tiles_cover_the_oracle_mask(swa, oracle_mod, n, w, g, r, BM, BN):
+    # the kernels' landmark tiles (swa_enumerate_landmark_tiles) carry exactly the
+    # landmark pairs the window tiles do not: mask(landmark) = mask(window) + those
+    full = oracle_mod.pattern_mask(n, w, g, r, "landmark").astype(bool)
+    win = oracle_mod.mask(n, w, g).astype(bool)
+    assert not (win & ~full).any()
+    extra = full & ~win                                   # pairs only the landmarks give
+    cols = np.arange(0, n, r)                             # landmark m sits at position r*m
+    assert not extra[:, np.setdiff1d(np.arange(n), cols)].any()
+    need = extra[:, cols]                                 # [n rows, ceil(n/r) landmarks]
+    nq, nk = -(-n // BM), -(-len(cols) // BN)
+    pad = np.zeros((nq * BM, nk * BN), dtype=bool)
+    pad[:n, :len(cols)] = need
+    rows_exist = np.zeros(nq * BM, dtype=bool)
+    rows_exist[:n] = True
+    ref = np.zeros((nq, nk), dtype=np.int32)
+    for qt in range(nq):
+        for lt in range(nk):
+            blk = pad[qt * BM:(qt + 1) * BM, lt * BN:(lt + 1) * BN]
+            ex = rows_exist[qt * BM:(qt + 1) * BM]
+            cnt = blk[ex].sum()
+            ref[qt, lt] = 0 if cnt == 0 else (2 if cnt == ex.sum() * BN else 1)
+    got = swa.enumerate_landmark_tiles(n, w, g, r, BM, BN).numpy()
+    # the last row of a query tile needs every landmark from ceil(g/r) up to its
+    # own limit, so the visited range holds no empty tile: classes match exactly
+    assert np.array_equal(got, ref)
