@@ -125,8 +125,15 @@ def peaks():
 
 
 def src_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of the SHA-256 of a source file's code, with comments
+    and blank lines removed: editing a comment keeps a capture valid, any change
+    to the code does not."""
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    code = "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def recorded_traffic(kernel, workload, src):

@@ -10,12 +10,16 @@
 // the walkthrough's section 1 last paragraph).
 //
 // Design (B300-native; the pages give no kernel):
+//  * Two kernels: the pair kernel (below; two query heads of a GQA group per
+//    work item, for even groups) and the single-head kernel described here
+//    (odd groups).
 //  * Persistent CTAs, one per SM.  A work item is (b, kv head, q tile of 128
-//    rows, query head of the group); items of one kv head are adjacent so the
-//    K/V band stays in L2 across the CTAs that run them together.
+//    rows, query head or head pair, residue class for the fixed patterns);
+//    items are ranked q tile first (decode_level_item), so the CTAs running at
+//    the same time share one band position of every kv head in L2.
 //  * Only key tiles (128 keys) that meet the band or the sink columns are
 //    visited (tile_range); the element mask is applied only on partial tiles.
-//  * Warp roles (192 threads):
+//  * Warp roles of the single-head kernel (192 threads):
 //      warp 0  TMA producer: Q tile (double-buffered), K and V tiles into a
 //              2-stage ring, 128-byte swizzled boxes of 64 columns.
 //      warp 1  MMA issuer: S = Q K^T (both operands from shared memory) into
@@ -669,18 +673,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 //
 // The two heads read the same key/value tiles, so each K/V tile staged in
 // shared memory feeds four MMAs (S_A, S_B, P_A V, P_B V) instead of two.  Two
-// softmax warpgroups (A: warps 2-5, B: warps 6-9) work on the two heads and
+// softmax warpgroups (A: warps 4-7, B: warps 8-11) work on the two heads and
 // take turns with the tensor core; the MMA warp issues, per key tile c,
 //     P_A(c-1) V, S_A(c) = Q_A K^T, P_B(c-1) V, S_B(c) = Q_B K^T
 // so softmax A(c) runs while the tensor core computes P_B(c-1) V and S_B(c),
 // and the other way round.  384 threads in three warpgroups: warpgroup 0 holds
 // the TMA warp (0) and the MMA warp (1) and gives registers away (setmaxnreg
-// down to 56), the softmax warpgroups 1 (warps 4-7, head A) and 2 (warps 8-11,
-// head B) take them (up to 224), so a full 128-column S row stays in registers.  TMEM (512 columns): O_A [0,128), S_A [128,256),
-// O_B [256,384), S_B [384,512); P (bf16) is written back over the first half
-// of its S buffer.  A tcgen05.commit tracks every MMA issued before it, so the
-// S_X(c) barrier also tells softmax X that P_X(c-1) V has landed in O_X and
-// that O_X may be rescaled.
+// down to REGS_CTRL), the softmax warpgroups take them (up to REGS_SOFTMAX), so
+// a full 128-column S row stays in registers.  TMEM (512 columns): O_A [0,128),
+// S_A [128,256), O_B [256,384), S_B [384,512); P (bf16) is written back over
+// the first half of its S buffer.  A tcgen05.commit tracks every MMA issued
+// before it, so the S_X(c) barrier also tells softmax X that P_X(c-1) V has
+// landed in O_X and that O_X may be rescaled.  Each softmax warp stages its
+// output rows through STAGE_WARP bytes of shared memory (store_o_rows).
 // ------------------------------------------------------------------------
 constexpr int NTHREADS2 = 384;
 // named barriers 1 (head A) and 2 (head B): a softmax warpgroup's 128 threads
