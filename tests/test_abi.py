@@ -119,6 +119,43 @@ def test_host_validation_rejects_before_launch(swa):
     assert L.swa_cache_append(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 2, 128, 8, 0, 0, None) == 0
 
 
+def test_pattern_and_chunk_validation_rejects_before_launch(swa):
+    L = swa.lib
+
+    def pattern(pat, w=8, g=0, r=4, n=64, d=128, H=4, Hkv=2, scale=0.1):
+        return L.swa_prefill_pattern(FAKE, FAKE, FAKE, FAKE, None, None, 1, H, Hkv, n, d, pat, w,
+                                     g, r, scale, 0, None)
+
+    assert pattern(7) == -1                   # no such pattern
+    assert pattern(1, r=0) == -1              # stride below one
+    assert pattern(2, r=-3) == -1
+    assert pattern(1, g=2) == -2              # the class patterns take no sinks
+    assert pattern(2, g=1) == -2
+    assert pattern(3, r=0) == -1
+    assert pattern(3, w=0) == -1
+    assert pattern(1, d=96) == -2
+    assert pattern(3, n=0) == -1
+    assert pattern(1, scale=float("inf")) == -1
+    assert pattern(0, w=0) == -1              # the window code is swa_prefill_sink_logit
+
+    B, H, Hkv, T, d, w, g = 2, 4, 2, 50, 128, 64, 4
+    need = L.swa_prefill_chunk_workspace_bytes(B, Hkv, T, d, w, g, 0)
+    # key lists of roundup(g+w-1, 128) + roundup(T, 128) rows for K and V, bf16
+    assert need == 2 * B * Hkv * (128 + 128) * d * 2
+    assert L.swa_prefill_chunk_workspace_bytes(B, Hkv, 0, d, w, g, 0) == 0
+
+    def chunk(T=T, ws=FAKE, ws_bytes=need, pos0=FAKE, append=1):
+        return L.swa_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, pos0, FAKE, None, None, B, H,
+                                   Hkv, T, d, w, g, 0.1, append, 0, ws, ws_bytes, None)
+
+    assert chunk(T=0) == -1
+    assert chunk(pos0=None) == -1
+    assert chunk(pos0=FAKE + 2) == -1         # pos0 not 4-byte aligned
+    assert chunk(ws=None) == -6
+    assert chunk(ws_bytes=need - 1) == -6
+    assert chunk(ws=FAKE + 8) == -6           # workspace not 16-byte aligned
+
+
 @pytest.mark.parametrize("n,w,g,r,BM,BN", [
     (300, 20, 0, 4, 32, 16), (500, 64, 3, 7, 64, 32), (257, 8, 9, 2, 16, 16),
     (1000, 100, 1, 50, 128, 128), (90, 200, 2, 5, 32, 8), (400, 30, 40, 8, 32, 32),
