@@ -29,6 +29,8 @@ DEC_CASES = [
     (2, 2, 2, 64, 100, 0, [99, 1000]),
     (1, 8, 1, 128, 33, 5, [35]),             # sinks still inside the window for some
     (4, 16, 2, 128, 300, 2, [301, 302, 1, 299]),
+    (2, 32, 16, 128, 128, 0, [500, 127]),    # GQA group of 2 (the Gemma-3 shape)
+    (3, 6, 3, 64, 40, 3, [2, 41, 3000]),     # group of 2, d = 64
 ]
 
 
@@ -124,3 +126,10 @@ def test_negative_position_is_reported(swa):
     assert swa.device_status() == -1  # SWA_ERR_INVALID_ARG, read from the device
     assert torch.isfinite(out.float()).all()
     assert swa.device_status() == 0   # cleared
+
+
+@pytest.mark.gpu
+def test_decode_group_of_16_is_refused(swa):
+    x = synthetic.decode_cache_inputs(1, 16, 1, 128, 8, 0, 9, seed=0, device="cuda")
+    with pytest.raises(swa.SwaError):
+        swa.decode(x.q, x.Kc, x.Vc, x.pos, 8, 0, x.scale, num_splits=1)

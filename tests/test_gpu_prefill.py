@@ -20,6 +20,9 @@ BF16_CASES = [
     (1, 2, 1, 2048, 128, 512, 0),    # mostly full tiles
     (1, 2, 1, 130, 128, 129, 1),
     (3, 4, 1, 200, 64, 17, 2),       # several sequences, GQA 4, d = 64
+    (1, 16, 1, 300, 128, 100, 2),    # group of 16: eight head pairs per kv head
+    (2, 5, 1, 260, 128, 70, 1),      # odd group of 5: single-head kernel
+    (2, 32, 16, 384, 128, 128, 0),   # the Gemma-3 head shape, window of one tile
 ]
 
 
