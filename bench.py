@@ -106,6 +106,35 @@ def chunk_flops(c):
     return 4 * keys * c["d"] * c["B"] * c["H"]
 
 
+def prefill_bytes(c, elem=2):
+    """Algorithmic HBM bytes of one prefill launch: Q, K, V read once, O written once."""
+    q = c["B"] * c["H"] * c["n"] * c["d"] * elem
+    kv = c["B"] * c["Hkv"] * c["n"] * c["d"] * elem
+    return 2 * q + 2 * kv
+
+
+def prefill_roofline(c, flops, launch_ms, pk, traffic, kernel):
+    """The roofline of one prefill launch: the tensor-core bound (useful FLOPs at
+    the measured bf16 peak) or, where the pattern reads few keys per query (the
+    strided head at s = sqrt(n)), the HBM bound (Q, K, V, O once at the measured
+    copy bandwidth), whichever takes longer."""
+    nbytes = prefill_bytes(c)
+    tflops = flops / (launch_ms * 1e-3) / 1e12
+    gbs = nbytes / (launch_ms * 1e-3) / 1e9
+    t_tensor = flops / (pk["bf16"] * 1e12)
+    t_hbm = nbytes / (pk["hbm"] * 1e9)
+    common = {"traffic": traffic, "kernel": kernel, "useful_flops_per_launch": flops,
+              "algorithmic_bytes": nbytes,
+              "tensor_bound_ms": t_tensor * 1e3, "hbm_bound_ms": t_hbm * 1e3}
+    if t_hbm > t_tensor:
+        return {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": gbs / pk["hbm"], "peak_source": pk["src"] + " copy",
+                "tensor_tflops": tflops, "tensor_frac": tflops / pk["bf16"], **common}
+    return {"bound": "tensor", "achieved": tflops, "peak": pk["bf16"], "unit": "TFLOP/s",
+            "frac": tflops / pk["bf16"], "peak_source": pk["src"] + " burst",
+            "frac_of_sustained": tflops / pk["bf16_sustained"], **common}
+
+
 def decode_bytes(c, elem=2):
     kv = c["B"] * c["Hkv"] * (c["w"] + c["g"]) * c["d"] * elem * 2
     qo = c["B"] * c["H"] * c["d"] * elem * 2
@@ -372,7 +401,7 @@ def run_swa(args):
     c = PREFILL_WORKLOADS[args.workload]
     flush = L2Flush(dev)
     flops = prefill_flops(c)
-    ms = value = achieved = traffic = kernel = None
+    ms = value = traffic = kernel = launch_ms = None
     clk_summary = None
     e2e = None
     if args.only in ("all", "prefill"):
@@ -398,7 +427,6 @@ def run_swa(args):
         ms = max_over_ranks(float(np.mean(times)), world, dev)
         value = flops * world / (ms * 1e-3) / 1e12
         launch_ms = float(np.mean(times))
-        achieved = flops / (launch_ms * 1e-3) / 1e12
         kernel = ("swa_prefill_bf16_pair_sm103" if (c["H"] // c["Hkv"]) % 2 == 0
                   else "swa_prefill_bf16_sm103")
         traffic = recorded_traffic(kernel, args.workload, PREFILL_KERNEL_SRC)
@@ -470,12 +498,8 @@ def run_swa(args):
         "clocks": clk_summary,
         "e2e": e2e,
         "gpu_launches": args.steps if value is not None else 0,
-        "roofline": None if value is None else {
-            "bound": "tensor", "achieved": achieved, "peak": pk["bf16"],
-            "unit": "TFLOP/s", "frac": achieved / pk["bf16"], "traffic": traffic,
-            "kernel": kernel, "peak_source": pk["src"] + " burst",
-            "frac_of_sustained": achieved / pk["bf16_sustained"],
-            "useful_flops_per_launch": flops},
+        "roofline": None if value is None else prefill_roofline(c, flops, launch_ms, pk,
+                                                                traffic, kernel),
         "cpu_baseline": cpu,
         "decode": decode_line,
     }

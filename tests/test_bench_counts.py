@@ -26,3 +26,18 @@ def test_window_flops_match_pair_count(oracle_mod):
         small = dict(c, n=3000, w=min(c["w"], 700))
         assert bench.prefill_flops(small) == 4 * oracle_mod.count_pairs(
             small["n"], small["w"], small["g"]) * c["d"] * c["B"] * c["H"]
+
+
+def test_roofline_bound_follows_the_larger_time():
+    pk = dict(bf16=1718.7, bf16_sustained=1400.0, hbm=6507.5, src="test")
+    # the Mistral-like layer is a dense contraction per tile: tensor-bound
+    c = bench.PREFILL_WORKLOADS["mistral_like_prefill"]
+    r = bench.prefill_roofline(c, bench.prefill_flops(c), 0.63, pk, None, "k")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["frac"] - bench.prefill_flops(c) / 0.63e-3 / 1e12 / 1718.7) < 1e-12
+    # the strided head at s = sqrt(n) reads ~n/2s keys per query: HBM-bound
+    c = bench.PREFILL_WORKLOADS["strided_prefill"]
+    r = bench.prefill_roofline(c, bench.prefill_flops(c), 0.33, pk, None, "k")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["algorithmic_bytes"] == 2 * (32 + 8) * 65536 * 128 * 2
+    assert r["hbm_bound_ms"] > r["tensor_bound_ms"]
