@@ -34,7 +34,8 @@
  *  - Arguments are validated on the host before any launch; an invalid call
  *    enqueues nothing and returns SWA_ERR_INVALID_ARG or SWA_ERR_UNSUPPORTED.
  *  - Entry points are thread-safe; the only library state is the decode
- *    workspace of swa_decode() and the per-device status word.
+ *    workspace of swa_decode(), the fixed scratch array of
+ *    swa_decode_noalloc() and the per-device status word.
  */
 #ifndef SWA_H
 #define SWA_H
@@ -186,6 +187,7 @@ int swa_prefill_chunk(const void *Q, const void *k_new, const void *v_new, void 
  * not yet written (pos < w-1) and sink slots of positions still inside the
  * window are not read.
  *   q [B][H][d], Kcache, Vcache [B][Hkv][w+g][d], O [B][H][d]: bf16, device.
+ *   The group size H/Hkv is 1, 2, 4 or 8 (SWA_ERR_UNSUPPORTED otherwise).
  * Split-K over the cached keys, then a log-sum-exp merge: a first kernel cuts
  * the cache rows of all (sequence, kv head) pairs, laid end to end, into equal
  * contiguous shares, one per CTA of a single resident wave, and writes one
