@@ -27,6 +27,10 @@ CASES = [
     ("landmark", 2, 4, 2, 900, 128, 64, 4, 50),     # with sinks; landmark 0 is a sink
     ("landmark", 1, 3, 1, 1300, 64, 128, 3, 2),     # a landmark every other position
     ("landmark", 1, 4, 2, 640, 128, 1000, 0, 7),    # window covers everything
+    # many classes per q-tile level (class-major item order), classes of 129 and
+    # 128 rows (two q tiles for some, one for the others)
+    ("strided", 8, 16, 16, 644, 64, 0, 0, 5),       # single-head kernel
+    ("dilated", 4, 32, 16, 1283, 64, 30, 0, 10),    # head pairs
 ]
 
 
