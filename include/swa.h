@@ -300,6 +300,20 @@ int swa_enumerate_tiles(int64_t n, int64_t w, int64_t g, int BM, int BN, int32_t
 int swa_enumerate_landmark_tiles(int64_t n, int64_t w, int64_t g, int64_t r, int BM, int BN,
                                  int32_t *cls, size_t cap);
 
+/*
+ * The key list a chunked prefill (swa_prefill_chunk) builds for a chunk of T
+ * tokens at positions pos0 .. pos0+T-1: position[r] is the token position
+ * whose key sits at index r of the list, or -1 for a padding row (the rows
+ * between the sinks and the window that align the chunk's queries with the
+ * 128-row tiles, and the rows past the list's end); query t of the chunk sits
+ * at index t + *query_offset.  The prefill kernels read index j for query
+ * index i when j <= i and (j >= i-w+1 or j < g).  `position` is host memory of
+ * `cap` int64 elements.  Returns the number of rows written (the workspace
+ * rows of swa_prefill_chunk_workspace_bytes), or SWA_ERR_INVALID_ARG.
+ */
+int swa_chunk_key_positions(int64_t pos0, int w, int g, int T, int64_t *position, size_t cap,
+                            int32_t *query_offset);
+
 /* Where the rolling cache keeps position p: *ring_slot = p mod w,
  * *sink_slot = w+p if p < g else -1.  Returns SWA_OK or SWA_ERR_INVALID_ARG. */
 int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_slot);

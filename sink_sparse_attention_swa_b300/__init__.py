@@ -22,7 +22,8 @@ import torch
 __all__ = [
     "SwaError", "prefill", "prefill_pattern", "prefill_chunk", "prefill_chunk_workspace_bytes",
     "PATTERNS", "decode", "cache_append", "decode_workspace_bytes",
-    "count_pairs", "enumerate_tiles", "enumerate_landmark_tiles", "cache_slot", "device_status",
+    "count_pairs", "enumerate_tiles", "enumerate_landmark_tiles", "chunk_key_positions",
+    "cache_slot", "device_status",
     "selftest_umma",
     "library_path", "lib",
 ]
@@ -56,6 +57,7 @@ SIGNATURES = {
     "swa_count_pairs": (_i64, [_i64, _i64, _i64]),
     "swa_enumerate_tiles": (_i, [_i64, _i64, _i64, _i, _i, _p, _sz]),
     "swa_enumerate_landmark_tiles": (_i, [_i64, _i64, _i64, _i64, _i, _i, _p, _sz]),
+    "swa_chunk_key_positions": (_i, [_i64, _i, _i, _i, _p, _sz, _p]),
     "swa_cache_slot": (_i, [_i64, _i, _i, _p, _p]),
     "swa_get_device_status": (_i, [_p]),
     "swa_status_string": (ctypes.c_char_p, [_i]),
@@ -317,6 +319,18 @@ def enumerate_landmark_tiles(n: int, w: int, g: int, r: int, BM: int, BN: int):
     rc = _load().swa_enumerate_landmark_tiles(n, w, g, r, BM, BN, out.data_ptr(), out.numel())
     _check("swa_enumerate_landmark_tiles", rc)
     return out
+
+
+def chunk_key_positions(pos0: int, w: int, g: int, T: int):
+    """(positions int64 [rows] with -1 for padding, query offset) of the key list a
+    chunked prefill builds; host-only."""
+    cap = ((g + w - 1 + 127) // 128 + (T + 127) // 128) * 128
+    pos = torch.empty(cap, dtype=torch.int64)
+    off = ctypes.c_int32(0)
+    rc = _load().swa_chunk_key_positions(int(pos0), int(w), int(g), int(T), pos.data_ptr(), cap,
+                                         ctypes.byref(off))
+    _check("swa_chunk_key_positions", rc if rc < 0 else 0)
+    return pos[:rc], int(off.value)
 
 
 def cache_slot(p: int, w: int, g: int):

@@ -312,6 +312,32 @@ int swa_enumerate_landmark_tiles(int64_t n, int64_t w, int64_t g, int64_t r, int
     return SWA_OK;
 }
 
+int swa_chunk_key_positions(int64_t pos0, int w, int g, int T, int64_t *position, size_t cap,
+                            int32_t *query_offset)
+{
+    if (pos0 < 0 || pos0 > INT32_MAX - static_cast<int64_t>(T) || w < 1 || g < 0 || T < 1 ||
+        position == nullptr || query_offset == nullptr ||
+        static_cast<long long>(w) + g > INT32_MAX)
+        return SWA_ERR_INVALID_ARG;
+    const long long rows = chunk_rows_max(w, g, T);
+    if (static_cast<unsigned long long>(rows) > cap) return SWA_ERR_INVALID_ARG;
+    const int ps = static_cast<int>(pos0);
+    const int S = chunk_sinks(ps, g), W0 = chunk_w0(ps, w, g), pad = chunk_pad(ps, w, g);
+    const long long L = static_cast<long long>(chunk_keys(ps, w, g, T));
+    for (long long r = 0; r < rows; ++r) {
+        int64_t v = -1;  // padding, or past the list
+        if (r < L) {
+            if (r < S)
+                v = r;
+            else if (r >= S + pad)
+                v = W0 + (r - S - pad);
+        }
+        position[r] = v;
+    }
+    *query_offset = chunk_offset(ps, w, g);
+    return static_cast<int>(rows);
+}
+
 int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_slot)
 {
     if (p < 0 || w < 1 || g < 0 || ring_slot == nullptr || sink_slot == nullptr)

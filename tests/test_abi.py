@@ -186,3 +186,31 @@ def test_landmark_tiles_cover_the_oracle_mask(swa, oracle_mod, n, w, g, r, BM, B
     # the last row of a query tile needs every landmark from ceil(g/r) up to its
     # own limit, so the visited range holds no empty tile: classes match exactly
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("pos0,w,g,T", [
+    (0, 64, 4, 50), (3, 64, 4, 50), (70, 64, 4, 50), (1000, 100, 2, 130), (99, 100, 2, 130),
+    (200, 37, 5, 1), (5, 37, 5, 1), (600, 300, 3, 257), (1, 1, 2, 40), (10, 1, 2, 40),
+    (300, 128, 0, 150), (50, 128, 0, 150), (100000, 4096, 4, 300), (4099, 4096, 4, 20),
+    (4, 8, 4, 3), (12, 8, 4, 1),
+])
+def test_chunk_key_list_reads_the_oracle_positions(swa, oracle_mod, pos0, w, g, T):
+    # the key list of a chunked prefill (the layout the gather kernel writes and the
+    # prefill kernels index): with the prefill mask applied to list indices, chunk
+    # query t reads exactly the positions the oracle's mask row pos0+t allows, each
+    # once, and never a padding row
+    pos, off = swa.chunk_key_positions(pos0, w, g, T)
+    pos = pos.numpy()
+    assert len(pos) % 128 == 0 and off + T <= len(pos)
+    for t in range(T):
+        i = t + off
+        j = np.arange(i + 1)
+        take = (j >= i - w + 1) | (j < g)
+        got = pos[j[take]]
+        assert (got >= 0).all(), (t, "reads a padding row")
+        assert len(set(got.tolist())) == len(got), (t, "reads a key twice")
+        want = np.nonzero(oracle_mod.mask_row(pos0 + t, pos0 + t + 1, w, g))[0]
+        assert sorted(got.tolist()) == want.tolist(), t
+    # the query offset is a multiple of the 128-row tile once the window has left the sinks
+    if pos0 >= g and pos0 - w + 1 >= g:
+        assert off % 128 == 0
