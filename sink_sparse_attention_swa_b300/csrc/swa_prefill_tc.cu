@@ -1368,7 +1368,7 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
                    const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
                    PrefillParams p, int per_unit, cudaStream_t stream)
 {
-    if (p.G % 2 == 0 && std::getenv("SWA_PREFILL_SINGLE") == nullptr) {
+    if (p.G % 2 == 0) {
         // two heads of a GQA pair per work item
         using L2 = Layout2<HD>;
         if (set_smem_once<swa_prefill_bf16_pair_sm103<HD, PAT>>(L2::DYN_SMEM) != cudaSuccess)
