@@ -8,8 +8,14 @@ and streams only).  The library is loaded on first use; if it is missing that
 first call raises ImportError: there is no fallback.
 
     prefill(q, k, v, w, g=0, scale=None, out=None, lse=None)        -> out
+    prefill_pattern(q, k, v, pattern, w, g=0, r=1, ...)             -> out
+    prefill_chunk(q, k_new, v_new, k_cache, v_cache, pos0, w, g=0,
+                  append=False, ...)                                -> out
     decode(q, k_cache, v_cache, pos, w, g=0, scale=None, ...)        -> out
     cache_append(k_cache, v_cache, k_new, v_new, pos0, w, g=0)
+
+The library is ``libswa.so`` next to this file, built in place by
+``build.py``; the environment variable SWA_LIBRARY names another copy.
 """
 from __future__ import annotations
 
