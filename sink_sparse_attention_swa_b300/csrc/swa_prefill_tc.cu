@@ -104,6 +104,9 @@ struct PrefillParams {
     // holds n_hi rows if c < rem, else n_lo; the last q-tile level holds
     // R_top classes (those with a row in it)
     int R, rem, n_hi, n_lo, R_top;
+    // pair kernel with an odd group: the two halves of an item are the q tiles
+    // 2k and 2k+1 of one query head (n_qt then counts pairs of q tiles)
+    int qpair;
     int rl;                  // landmark stride, 0 for none
     float sl2;  // scale * log2(e)
     __nv_bfloat16 *O;
@@ -167,7 +170,9 @@ __device__ __forceinline__ TileRange item_tiles(const PrefillParams &p, int b, i
         off = chunk_offset(ps < 0 ? 0 : ps, p.w, p.g);
     }
     const int nq = !PAT ? p.n : cls < p.rem ? p.n_hi : p.n_lo;
-    const int q0 = qt * BM, q1 = (q0 + BM < nq ? q0 + BM : nq) - 1;
+    // with q-tile pairs the walk covers the key tiles of both q tiles
+    const int rows = (!PAT && p.qpair) ? 2 * BM : BM;
+    const int q0 = qt * rows, q1 = (q0 + rows < nq ? q0 + rows : nq) - 1;
     TileRange tr = tile_range_at(q0 + off, q1 + off, p.w, p.g, BN);
     if constexpr (PAT) add_landmarks(tr, p.w, p.g, p.rl, BN);
     return tr;
@@ -264,6 +269,17 @@ __device__ __forceinline__ void store_o_rows(uint32_t o_addr, float inv_l,
         }
         __syncwarp();
     }
+}
+
+// Units of the pair kernel per kv head: head pairs of an even group, or single
+// heads whose two halves are two q tiles (odd groups); and the head of half x.
+__device__ __forceinline__ int pair_units(const PrefillParams &p)
+{
+    return p.qpair ? p.G : (p.G >> 1);
+}
+__device__ __forceinline__ int pair_head(const PrefillParams &p, int kvh, int u, int x)
+{
+    return p.qpair ? kvh * p.G + u : kvh * p.G + 2 * u + x;
 }
 
 // One box of rows: with the fixed patterns through the 4-D views (class
@@ -862,8 +878,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
                  t = pair_item_rank(blockIdx.x, ++it)) {
                 int b, hp, kvh, qt, cls;
-                decode_level_item<PAT>(t, p, p.G >> 1, b, hp, kvh, qt, cls);
-                const int h0 = kvh * p.G + 2 * hp;
+                decode_level_item<PAT>(t, p, pair_units(p), b, hp, kvh, qt, cls);
                 int off;
                 const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
                 const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
@@ -874,9 +889,11 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         break;
                     }
                     mbar_expect_tx(BAR(L::Q_FULL + x), L::QB);
+                    const int hx = pair_head(p, kvh, hp, x);
+                    const int qrow = (!PAT && p.qpair) ? (2 * qt + x) * BM : qt * BM;
                     for (int c = 0; c < HD / 64; ++c)
                         load_rows<PAT>(sQ + x * L::QB + c * (BM * 128), mq, BAR(L::Q_FULL + x),
-                                       c * 64, cls, qt * BM, b * p.H + h0 + x);
+                                       c * 64, cls, qrow, b * p.H + hx);
                     last_q_par[x] = it & 1;
                 }
                 for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
@@ -973,7 +990,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
                  t = pair_item_rank(blockIdx.x, ++it)) {
                 int b, hp, kvh, qt, cls;
-                decode_level_item<PAT>(t, p, p.G >> 1, b, hp, kvh, qt, cls);
+                decode_level_item<PAT>(t, p, pair_units(p), b, hp, kvh, qt, cls);
                 int off;
                 const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
                 for (int j = 0; j < tr.count; ++j, ++kv_iter, ++c) {
@@ -1040,8 +1057,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         };
         auto load_item = [&](int t, Item &e) {
             int hp, kvh, qt;
-            decode_level_item<PAT>(t, p, p.G >> 1, e.b, hp, kvh, qt, e.cls);
-            e.h = kvh * p.G + 2 * hp + x;
+            decode_level_item<PAT>(t, p, pair_units(p), e.b, hp, kvh, qt, e.cls);
+            e.h = pair_head(p, kvh, hp, x);
             e.tr = item_tiles<PAT>(p, e.b, qt, e.cls, e.off);
         };
         Item nxt;
@@ -1050,7 +1067,16 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         while (ok && t < pairs_per_item_count) {
             const int b = nxt.b, h = nxt.h, cls = nxt.cls, off = nxt.off;
             const TileRange tr = nxt.tr;
-            const int i = tr.q0 + r;
+            // this half's own rows: with q-tile pairs, half x is q tile 2k + x,
+            // and tiles of the walk are classed (full or not) against its rows
+            const bool qp = !PAT && p.qpair;
+            TileRange trx = tr;
+            if (qp) {
+                trx.q0 = tr.q0 + x * BM;
+                const int e1 = trx.q0 + BM - 1;
+                trx.q1 = e1 < tr.q1 ? e1 : tr.q1;
+            }
+            const int i = trx.q0 + r;
             const int lo = i - p.w + 1;
             const int lhi = PAT ? land_hi(i, p.w, p.rl > 0 ? p.rl : 1) : 0;
             const int llo = PAT && p.rl > 0 ? land_lo(p.g, p.rl) : 0;
@@ -1068,7 +1094,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) reg_fence32(s[q]);
                 const KeyTile kt = key_tile<PAT>(tr, j, p);
-                if (!kt.full) {
+                const bool full = qp ? tile_full(trx, kt.k0 / BN, p.w, p.g, BN) : kt.full;
+                if (!full) {
                     // band and sink tiles: k <= i and (k >= i-w+1 or k < g); landmark
                     // tiles (k a landmark index): land_lo <= k <= land_hi(i)
                     const int khi = kt.land ? lhi : i, klo = kt.land ? llo : lo;
@@ -1368,12 +1395,19 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
                    const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
                    PrefillParams p, int per_unit, cudaStream_t stream)
 {
-    if (p.G % 2 == 0) {
-        // two heads of a GQA pair per work item
+    // an odd group runs the pair kernel on pairs of q tiles of one head (the
+    // plain window path; the fixed patterns keep the single-head kernel)
+    p.qpair = (!PAT && p.G % 2 != 0) ? 1 : 0;
+    if (p.G % 2 == 0 || p.qpair) {
+        // two heads of a GQA pair, or two q tiles of one head, per work item
         using L2 = Layout2<HD>;
         if (set_smem_once<swa_prefill_bf16_pair_sm103<HD, PAT>>(L2::DYN_SMEM) != cudaSuccess)
             return SWA_ERR_CUDA;
-        p.num_items = p.B * p.Hkv * (p.G / 2) * per_unit;
+        if (p.qpair) {
+            p.n_qt = (p.n + 2 * BM - 1) / (2 * BM);  // levels of q-tile pairs
+            per_unit = p.n_qt;
+        }
+        p.num_items = p.B * p.Hkv * (p.qpair ? p.G : p.G / 2) * per_unit;
         const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
         swa_prefill_bf16_pair_sm103<HD, PAT>
             <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
