@@ -11,8 +11,9 @@
 //
 // Design (B300-native; the pages give no kernel):
 //  * Two kernels: the pair kernel (below; two query heads of a GQA group per
-//    work item, for even groups) and the single-head kernel described here
-//    (odd groups).
+//    work item for even groups, two adjacent q tiles of one head for odd
+//    groups) and the single-head kernel described here (odd groups under the
+//    fixed patterns).
 //  * Persistent CTAs, one per SM.  A work item is (b, kv head, q tile of 128
 //    rows, query head or head pair, residue class for the fixed patterns);
 //    items are ranked q tile first (decode_level_item), so the CTAs running at
