@@ -105,9 +105,6 @@ struct PrefillParams {
     // holds n_hi rows if c < rem, else n_lo; the last q-tile level holds
     // R_top classes (those with a row in it)
     int R, rem, n_hi, n_lo, R_top;
-    // pair kernel with an odd group: the two halves of an item are the q tiles
-    // 2k and 2k+1 of one query head (n_qt then counts pairs of q tiles)
-    int qpair;
     int rl;                  // landmark stride, 0 for none
     float sl2;  // scale * log2(e)
     __nv_bfloat16 *O;
@@ -161,7 +158,9 @@ __device__ __forceinline__ void decode_level_item(int r, const PrefillParams &p,
 // indices; *off is the list index of query row 0 (0 for a plain prefill,
 // chunk_offset(pos0[b]) for a chunked one).  With residue classes, rows and
 // keys are indices into the class's subsequence.
-template <bool PAT>
+// QP: the item is a pair of q tiles of one head (the pair kernel on an odd
+// group; n_qt then counts pairs of q tiles)
+template <bool PAT, bool QP = false>
 __device__ __forceinline__ TileRange item_tiles(const PrefillParams &p, int b, int qt, int cls,
                                                 int &off)
 {
@@ -172,7 +171,7 @@ __device__ __forceinline__ TileRange item_tiles(const PrefillParams &p, int b, i
     }
     const int nq = !PAT ? p.n : cls < p.rem ? p.n_hi : p.n_lo;
     // with q-tile pairs the walk covers the key tiles of both q tiles
-    const int rows = (!PAT && p.qpair) ? 2 * BM : BM;
+    const int rows = QP ? 2 * BM : BM;
     const int q0 = qt * rows, q1 = (q0 + rows < nq ? q0 + rows : nq) - 1;
     TileRange tr = tile_range_at(q0 + off, q1 + off, p.w, p.g, BN);
     if constexpr (PAT) add_landmarks(tr, p.w, p.g, p.rl, BN);
@@ -274,13 +273,15 @@ __device__ __forceinline__ void store_o_rows(uint32_t o_addr, float inv_l,
 
 // Units of the pair kernel per kv head: head pairs of an even group, or single
 // heads whose two halves are two q tiles (odd groups); and the head of half x.
+template <bool QP>
 __device__ __forceinline__ int pair_units(const PrefillParams &p)
 {
-    return p.qpair ? p.G : (p.G >> 1);
+    return QP ? p.G : (p.G >> 1);
 }
+template <bool QP>
 __device__ __forceinline__ int pair_head(const PrefillParams &p, int kvh, int u, int x)
 {
-    return p.qpair ? kvh * p.G + u : kvh * p.G + 2 * u + x;
+    return QP ? kvh * p.G + u : kvh * p.G + 2 * u + x;
 }
 
 // One box of rows: with the fixed patterns through the 4-D views (class
@@ -810,7 +811,7 @@ __device__ __forceinline__ void softmax_half(const uint32_t (&sa)[32], const uin
     }
 }
 
-template <int HD, bool PAT>
+template <int HD, bool PAT, bool QP>
 __global__ void __launch_bounds__(NTHREADS2, 1)
     swa_prefill_bf16_pair_sm103(const __grid_constant__ CUtensorMap tmQ,
                                 const __grid_constant__ CUtensorMap tmK,
@@ -879,9 +880,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
                  t = pair_item_rank(blockIdx.x, ++it)) {
                 int b, hp, kvh, qt, cls;
-                decode_level_item<PAT>(t, p, pair_units(p), b, hp, kvh, qt, cls);
+                decode_level_item<PAT>(t, p, pair_units<QP>(p), b, hp, kvh, qt, cls);
                 int off;
-                const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
+                const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
                 const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
                 for (int x = 0; x < 2 && ok; ++x) {
                     if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
@@ -890,8 +891,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         break;
                     }
                     mbar_expect_tx(BAR(L::Q_FULL + x), L::QB);
-                    const int hx = pair_head(p, kvh, hp, x);
-                    const int qrow = (!PAT && p.qpair) ? (2 * qt + x) * BM : qt * BM;
+                    const int hx = pair_head<QP>(p, kvh, hp, x);
+                    const int qrow = QP ? (2 * qt + x) * BM : qt * BM;
                     for (int c = 0; c < HD / 64; ++c)
                         load_rows<PAT>(sQ + x * L::QB + c * (BM * 128), mq, BAR(L::Q_FULL + x),
                                        c * 64, cls, qrow, b * p.H + hx);
@@ -991,9 +992,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
                  t = pair_item_rank(blockIdx.x, ++it)) {
                 int b, hp, kvh, qt, cls;
-                decode_level_item<PAT>(t, p, pair_units(p), b, hp, kvh, qt, cls);
+                decode_level_item<PAT>(t, p, pair_units<QP>(p), b, hp, kvh, qt, cls);
                 int off;
-                const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
+                const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
                 for (int j = 0; j < tr.count; ++j, ++kv_iter, ++c) {
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
@@ -1058,9 +1059,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         };
         auto load_item = [&](int t, Item &e) {
             int hp, kvh, qt;
-            decode_level_item<PAT>(t, p, pair_units(p), e.b, hp, kvh, qt, e.cls);
-            e.h = pair_head(p, kvh, hp, x);
-            e.tr = item_tiles<PAT>(p, e.b, qt, e.cls, e.off);
+            decode_level_item<PAT>(t, p, pair_units<QP>(p), e.b, hp, kvh, qt, e.cls);
+            e.h = pair_head<QP>(p, kvh, hp, x);
+            e.tr = item_tiles<PAT, QP>(p, e.b, qt, e.cls, e.off);
         };
         Item nxt;
         int t = pair_item_rank(blockIdx.x, 0);
@@ -1070,9 +1071,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             const TileRange tr = nxt.tr;
             // this half's own rows: with q-tile pairs, half x is q tile 2k + x,
             // and tiles of the walk are classed (full or not) against its rows
-            const bool qp = !PAT && p.qpair;
+            constexpr bool qp = QP;
             TileRange trx = tr;
-            if (qp) {
+            if constexpr (qp) {
                 trx.q0 = tr.q0 + x * BM;
                 const int e1 = trx.q0 + BM - 1;
                 trx.q1 = e1 < tr.q1 ? e1 : tr.q1;
@@ -1396,21 +1397,28 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
                    const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
                    PrefillParams p, int per_unit, cudaStream_t stream)
 {
-    // an odd group runs the pair kernel on pairs of q tiles of one head (the
-    // plain window path; the fixed patterns keep the single-head kernel)
-    p.qpair = (!PAT && p.G % 2 != 0) ? 1 : 0;
-    if (p.G % 2 == 0 || p.qpair) {
-        // two heads of a GQA pair, or two q tiles of one head, per work item
-        using L2 = Layout2<HD>;
-        if (set_smem_once<swa_prefill_bf16_pair_sm103<HD, PAT>>(L2::DYN_SMEM) != cudaSuccess)
+    using L2 = Layout2<HD>;
+    if (p.G % 2 == 0) {
+        // two heads of a GQA pair per work item
+        if (set_smem_once<swa_prefill_bf16_pair_sm103<HD, PAT, false>>(L2::DYN_SMEM) !=
+            cudaSuccess)
             return SWA_ERR_CUDA;
-        if (p.qpair) {
-            p.n_qt = (p.n + 2 * BM - 1) / (2 * BM);  // levels of q-tile pairs
-            per_unit = p.n_qt;
-        }
-        p.num_items = p.B * p.Hkv * (p.qpair ? p.G : p.G / 2) * per_unit;
+        p.num_items = p.B * p.Hkv * (p.G / 2) * per_unit;
         const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-        swa_prefill_bf16_pair_sm103<HD, PAT>
+        swa_prefill_bf16_pair_sm103<HD, PAT, false>
+            <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
+        return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+    }
+    if constexpr (!PAT) {
+        // an odd group: two adjacent q tiles of one head per work item (the
+        // fixed patterns keep the single-head kernel below)
+        if (set_smem_once<swa_prefill_bf16_pair_sm103<HD, false, true>>(L2::DYN_SMEM) !=
+            cudaSuccess)
+            return SWA_ERR_CUDA;
+        p.n_qt = (p.n + 2 * BM - 1) / (2 * BM);  // levels of q-tile pairs
+        p.num_items = p.B * p.H * p.n_qt;
+        const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
+        swa_prefill_bf16_pair_sm103<HD, false, true>
             <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
         return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
     }
