@@ -45,6 +45,8 @@ PREFILL_WORKLOADS = {
     # the full-causal global layer of the Gemma-3 hybrid (w >= n)
     "gemma3_global_prefill": dict(B=2, H=32, Hkv=16, n=32768, d=128, w=32768, g=0,
                                   sink_scale=1.0),
+    # plain multi-head attention (odd group: q-tile pairs in the pair kernel)
+    "mha_prefill": dict(B=1, H=32, Hkv=32, n=16384, d=128, w=4096, g=0, sink_scale=1.0),
     # other fixed patterns (swa_prefill_pattern)
     "dilated_prefill": dict(B=1, H=32, Hkv=8, n=16384, d=128, w=1024, g=0, sink_scale=1.0,
                             pattern="dilated", r=4),

@@ -15,6 +15,8 @@ Workloads (the shapes come from the model families the pages quote):
                           sink keys (positions 0..3) scaled x4
   gemma3_global_prefill   B=2 H=32 Hkv=16 n=32768 d=128 w=n (full causal) g=0,
                           bf16: the global layer between the local ones
+  mha_prefill             B=1 H=Hkv=32 n=16384 d=128 w=4096 g=0, bf16: plain
+                          multi-head attention (a group of one)
   dilated_prefill         B=1 H=32 Hkv=8 n=16384 d=128, dilated window w=1024
                           r=4 (the reach of a 4096 window at a quarter of it)
   strided_prefill         B=1 H=32 Hkv=8 n=65536 d=128, Sparse Transformer
@@ -45,6 +47,8 @@ WORKLOADS = {
                               g=4, dtype="bf16", sink_scale=4.0),
     "gemma3_global_prefill": dict(kind="prefill", B=2, H=32, Hkv=16, n=32768, d=128, w=32768,
                                   g=0, dtype="bf16", sink_scale=1.0),
+    "mha_prefill": dict(kind="prefill", B=1, H=32, Hkv=32, n=16384, d=128, w=4096, g=0,
+                        dtype="bf16", sink_scale=1.0),
     "dilated_prefill": dict(kind="prefill", B=1, H=32, Hkv=8, n=16384, d=128, w=1024, g=0,
                             dtype="bf16", sink_scale=1.0, pattern="dilated", r=4),
     "strided_prefill": dict(kind="prefill", B=1, H=32, Hkv=8, n=65536, d=128, w=0, g=0,

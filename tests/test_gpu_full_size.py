@@ -8,6 +8,7 @@ Workloads (inputs seeded exactly as the benchmark seeds them):
   gemma3_local_prefill   B=2 H=32 Hkv=16 n=32768  d=128 w=1024 g=0
   long_sink_prefill      B=1 H=32 Hkv=8  n=131072 d=128 w=4096 g=4, sink keys x4
   gemma3_global_prefill  B=2 H=32 Hkv=16 n=32768  d=128 w=n (full causal) g=0
+  mha_prefill            B=1 H=32 Hkv=32 n=16384  d=128 w=4096 g=0 (a group of one)
   dilated_prefill        B=1 H=32 Hkv=8  n=16384  d=128 dilated w=1024 r=4
   strided_prefill        B=1 H=32 Hkv=8  n=65536  d=128 strided r=256
   landmark_prefill       B=1 H=32 Hkv=8  n=16384  d=128 w=4096 g=4 landmarks r=64
@@ -31,7 +32,7 @@ def edge_rows(B, H, n, w, g):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", ["mistral_like_prefill", "gemma3_local_prefill",
-                                  "long_sink_prefill", "gemma3_global_prefill",
+                                  "long_sink_prefill", "gemma3_global_prefill", "mha_prefill",
                                   "dilated_prefill", "strided_prefill", "landmark_prefill"])
 def test_prefill_full_size_sampled_rows(swa, oracle_mod, name):
     c = synthetic.WORKLOADS[name]
