@@ -33,9 +33,17 @@
  *    clears it.
  *  - Arguments are validated on the host before any launch; an invalid call
  *    enqueues nothing and returns SWA_ERR_INVALID_ARG or SWA_ERR_UNSUPPORTED.
- *  - Entry points are thread-safe; the only library state is the decode
- *    workspace of swa_decode(), the fixed scratch array of
- *    swa_decode_noalloc() and the per-device status word.
+ *  - Threads.  Every entry point may be called from several host threads at
+ *    once.  The library's own state is small: the decode workspaces of
+ *    swa_decode() (one per device and stream, see there), the fixed scratch
+ *    array of swa_decode_noalloc() (one per device, shared by every call),
+ *    the per-device status word and per-device launch settings.  Calls whose
+ *    buffers are all the caller's (prefill, swa_decode_ex with a workspace of
+ *    its own, append) never share memory with one another.  swa_decode() calls
+ *    on different streams use different workspaces; calls on one stream are
+ *    ordered by that stream.  swa_decode_noalloc() calls all share one array:
+ *    calls whose kernels overlap on the GPU race and must be serialised by
+ *    the caller (one stream, or events).
  */
 #ifndef SWA_H
 #define SWA_H
@@ -192,9 +200,13 @@ int swa_prefill_chunk(const void *Q, const void *k_new, const void *v_new, void 
  * the cache rows of all (sequence, kv head) pairs, laid end to end, into equal
  * contiguous shares, one per CTA of a single resident wave, and writes one
  * partial (max, sum, unnormalised output) per share and pair; a second kernel
- * merges them.  Uses a library-owned workspace that grows on demand
- * (cudaMalloc on first use of a size, so make the first call outside stream
- * capture).
+ * merges them.  Uses a library-owned workspace, one per (device, stream)
+ * (per calling thread too for cudaStreamPerThread), so calls on different
+ * streams may overlap safely.  A workspace grows on demand (cudaMalloc when a
+ * stream first needs more, so make the first call of a size on a stream
+ * outside stream capture); an outgrown buffer is kept, not freed, until the
+ * process exits, because kernels or captured graphs may still use it.  Returns
+ * SWA_ERR_ALLOC, enqueuing nothing, if that allocation fails.
  */
 int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos,
                int B, int H, int Hkv, int d, int w, int g, float scale, void *O,
@@ -233,7 +245,10 @@ int swa_decode_sink_logit(const void *q, const void *Kcache, const void *Vcache,
  * Attention, from Longformer to CSA2", section 2: position i overwrites slot
  * i mod w; "Local and Sparse Attention: Reading Fewer Token Positions",
  * Figure 4).  Writes T new tokens k_new, v_new [B][Hkv][T][d] of sequence b at
- * positions pos0[b] .. pos0[b]+T-1 (pos0: device int32 [B], >= 0): position p
+ * positions pos0[b] .. pos0[b]+T-1 (pos0: device int32 [B], 0 <= pos0[b] <=
+ * INT32_MAX - T; a sequence whose pos0[b] is outside that range is left
+ * untouched and marks the device status word, which swa_get_device_status()
+ * then reports as SWA_ERR_INVALID_ARG): position p
  * goes to ring slot p mod w and, if p < g, also to sink slot w+p.  When T > w
  * only the last w positions are written to the ring (earlier ones would be
  * overwritten anyway); sink slots are written for every p < g.
@@ -323,8 +338,31 @@ int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_sl
 /* ---------------------------------------------------------------------- */
 
 /* Synchronises `stream`, then reads and clears the current device's status
- * word: SWA_OK, SWA_ERR_DEVICE_TIMEOUT, or SWA_ERR_CUDA if a CUDA call failed. */
+ * word: SWA_OK; SWA_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out;
+ * SWA_ERR_INVALID_ARG if a decode, append or chunked prefill met a position
+ * outside its range (negative, or past INT32_MAX); SWA_ERR_CUDA if a CUDA call
+ * failed. */
 int swa_get_device_status(swa_stream_t stream);
+
+/*
+ * swa_debug_inject_stall -- a test aid with no counterpart on the pages; it
+ * lets a test run the kernels' timeout path without faulting or hanging the
+ * GPU.  The next launch of the chosen kind on the current device leaves out
+ * its first key/value copy and gives each of its bounded waits `wait_ns`
+ * nanoseconds instead of 2 s:
+ *   kind 1 (SWA_STALL_PREFILL): the next bf16 prefill launch (swa_prefill*,
+ *           swa_prefill_pattern, the attention of swa_prefill_chunk);
+ *   kind 2 (SWA_STALL_DECODE):  the next decode split pass (swa_decode*).
+ * A wait of that launch then runs out: the kernel stops early, waits for the
+ * copies it did start, frees its tensor memory, and marks the device status
+ * word, so swa_get_device_status() returns SWA_ERR_DEVICE_TIMEOUT.  That
+ * launch's outputs are unspecified; later launches are unaffected.  The
+ * setting is used once; kind 0 cancels a pending one.  wait_ns must be in
+ * [1e5, 2e9].  Returns SWA_OK, SWA_ERR_INVALID_ARG or SWA_ERR_CUDA.
+ */
+#define SWA_STALL_PREFILL 1
+#define SWA_STALL_DECODE 2
+int swa_debug_inject_stall(int kind, int64_t wait_ns);
 
 /* A static string naming a swa_status value. */
 const char *swa_status_string(int status);

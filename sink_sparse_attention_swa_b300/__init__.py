@@ -29,7 +29,7 @@ __all__ = [
     "SwaError", "prefill", "prefill_pattern", "prefill_chunk", "prefill_chunk_workspace_bytes",
     "PATTERNS", "decode", "cache_append", "decode_workspace_bytes",
     "count_pairs", "enumerate_tiles", "enumerate_landmark_tiles", "chunk_key_positions",
-    "cache_slot", "device_status",
+    "cache_slot", "device_status", "inject_stall",
     "selftest_umma",
     "library_path", "lib",
 ]
@@ -66,6 +66,7 @@ SIGNATURES = {
     "swa_chunk_key_positions": (_i, [_i64, _i, _i, _i, _p, _sz, _p]),
     "swa_cache_slot": (_i, [_i64, _i, _i, _p, _p]),
     "swa_get_device_status": (_i, [_p]),
+    "swa_debug_inject_stall": (_i, [_i, _i64]),
     "swa_status_string": (ctypes.c_char_p, [_i]),
     "swa_version": (_i, []),
     "swa_selftest_umma": (_i, [_p, _p, _p, _p, _p, _p]),
@@ -348,6 +349,17 @@ def cache_slot(p: int, w: int, g: int):
 def device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status code."""
     return int(_load().swa_get_device_status(_stream(stream, None)))
+
+
+STALL_KINDS = {"prefill": 1, "decode": 2}
+
+
+def inject_stall(kind: str, wait_ns: int = 1_000_000) -> None:
+    """Test aid (swa_debug_inject_stall): the next prefill ("prefill") or decode
+    split pass ("decode") launched on the current device leaves out its first
+    key/value copy and waits at most wait_ns per bounded wait, so its timeout
+    path runs; device_status() then returns -4 (SWA_ERR_DEVICE_TIMEOUT)."""
+    _check("swa_debug_inject_stall", _load().swa_debug_inject_stall(STALL_KINDS[kind], int(wait_ns)))
 
 
 def selftest_umma(A, Bk, Bn, stream=None):

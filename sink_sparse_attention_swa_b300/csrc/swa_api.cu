@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <thread>
+#include <vector>
 
 #include "swa_internal.h"
 
@@ -27,12 +29,62 @@ int check_heads(int B, int H, int Hkv, int d, int w, int g)
     return SWA_OK;
 }
 
-struct Workspace {
-    void *ptr = nullptr;
-    size_t bytes = 0;
+// The library-owned decode workspace of swa_decode: one buffer per (device,
+// stream), so calls on different streams never share partials.  The per-thread
+// default stream has one handle for every thread, so that handle is keyed by
+// the calling thread too.  A buffer that is outgrown is retired, not freed: a
+// kernel enqueued earlier may still read it, and a CUDA graph captured earlier
+// may still name it.  Retired buffers are kept until the process exits (the
+// sizes grow at least twofold, so they add up to less than the live one).
+struct StreamWorkspace {
+    cudaStream_t stream;
+    std::thread::id thread;
+    void *ptr;
+    size_t bytes;
+};
+struct DeviceWorkspaces {
+    std::vector<StreamWorkspace> live;
+    std::vector<void *> retired;
 };
 std::mutex g_ws_mu;
-Workspace g_ws[64];
+DeviceWorkspaces g_ws[kMaxDevices];
+
+// Returns a workspace of at least `need` bytes for (current device, stream),
+// growing it if needed; nullptr with *rc set on failure.  Called with g_ws_mu
+// held.
+void *stream_workspace(cudaStream_t stream, size_t need, int *rc)
+{
+    const int dev = current_device();
+    if (dev < 0) {
+        *rc = SWA_ERR_CUDA;
+        return nullptr;
+    }
+    const std::thread::id tid =
+        stream == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id();
+    DeviceWorkspaces &D = g_ws[dev];
+    StreamWorkspace *W = nullptr;
+    for (auto &e : D.live)
+        if (e.stream == stream && e.thread == tid) W = &e;
+    if (W == nullptr) {
+        D.live.push_back(StreamWorkspace{stream, tid, nullptr, 0});
+        W = &D.live.back();
+    }
+    if (W->bytes < need) {
+        const size_t grow = need > 2 * W->bytes ? need : 2 * W->bytes;
+        void *p = nullptr;
+        if (cudaMalloc(&p, grow) != cudaSuccess) {
+            // clear the runtime's last-error state, so that the next launch's
+            // error check does not report this failure as its own
+            (void)cudaGetLastError();
+            *rc = SWA_ERR_ALLOC;
+            return nullptr;
+        }
+        if (W->ptr != nullptr) D.retired.push_back(W->ptr);
+        W->ptr = p;
+        W->bytes = grow;
+    }
+    return W->ptr;
+}
 
 }  // namespace
 
@@ -216,28 +268,12 @@ int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int3
     int rc = check_heads(B, H, Hkv, d, w, g);
     if (rc != SWA_OK) return rc;
     const size_t need = decode_workspace_bytes(B, H, Hkv, d, decode_ctas(B, Hkv, w, g, 0));
-    void *ws = nullptr;
-    {
-        int dev = -1;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SWA_ERR_CUDA;
-        std::lock_guard<std::mutex> lk(g_ws_mu);
-        Workspace &W = g_ws[dev];
-        if (W.bytes < need) {
-            if (W.ptr != nullptr) {
-                // the old buffer may still be read by an earlier launch
-                if (cudaDeviceSynchronize() != cudaSuccess) return SWA_ERR_CUDA;
-                cudaFree(W.ptr);
-                W.ptr = nullptr;
-                W.bytes = 0;
-            }
-            if (cudaMalloc(&W.ptr, need) != cudaSuccess) {
-                W.ptr = nullptr;
-                return SWA_ERR_ALLOC;
-            }
-            W.bytes = need;
-        }
-        ws = W.ptr;
-    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the lock is held until both kernels are enqueued, so the table is never
+    // changed under a call that is still choosing its buffer
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    void *ws = stream_workspace(st, need, &rc);
+    if (ws == nullptr) return rc;
     return swa_decode_ex(q, Kcache, Vcache, pos, B, H, Hkv, d, w, g, scale, O, nullptr, SWA_BF16, 0,
                          ws, need, stream);
 }
@@ -346,6 +382,8 @@ int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_sl
     *sink_slot = (p < g) ? static_cast<int32_t>(w + p) : -1;
     return SWA_OK;
 }
+
+int swa_debug_inject_stall(int kind, int64_t wait_ns) { return set_injected_stall(kind, wait_ns); }
 
 int swa_get_device_status(swa_stream_t stream)
 {

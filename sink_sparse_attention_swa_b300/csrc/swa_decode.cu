@@ -160,6 +160,8 @@ struct DecodeParams {
     void *O;        // [B][H][d]
     float *lse;     // [B][H] or null
     const float *sink;  // per-head sink logits [H] or null
+    uint64_t wait_ns;   // limit of every bounded wait of the roles (2 s unless a test sets it)
+    int skip_first_stage;  // test injection: the first stage's copies are left out (see swa.h)
 };
 
 __host__ __device__ __forceinline__ long long cta_begin(long long T, int P, int c)
@@ -188,12 +190,13 @@ __device__ __forceinline__ Seg make_seg(const DecodeParams &p, long long bk, int
     s.bk = static_cast<int>(bk);
     s.b = static_cast<int>(bk / p.Hkv);
     s.kvh = static_cast<int>(bk % p.Hkv);
-    int pos = __ldg(p.pos + s.b);
+    // 64-bit: pos may be as large as INT32_MAX
+    long long pos = __ldg(p.pos + s.b);
     s.bad_pos = pos < 0;
     if (pos < 0) pos = -1;
-    const int nring = pos + 1 < p.w ? pos + 1 : p.w;
-    int nsink = pos - p.w + 1;
-    nsink = nsink < 0 ? 0 : (nsink > p.g ? p.g : nsink);
+    const int nring = static_cast<int>(pos + 1 < p.w ? pos + 1 : p.w);
+    long long ns = pos - p.w + 1;
+    const int nsink = static_cast<int>(ns < 0 ? 0 : (ns > p.g ? p.g : ns));
     s.ring_lo = t0;
     s.ring_hi = t1 < nring ? t1 : nring;
     s.sink_lo = t0 > p.w ? t0 : p.w;
@@ -290,8 +293,11 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
             [&](int it, const Seg &s, int row, int count) -> bool {
                 const int slot = it % C::NS;
                 const uint32_t ph = (it / C::NS) & 1;
-                if (!mbar_wait(EMPTY(slot), ph ^ 1, abort_flag, p.status, DEC_TIMEOUT_NS))
+                if (!mbar_wait(EMPTY(slot), ph ^ 1, abort_flag, p.status, p.wait_ns))
                     return false;
+                // test injection: this stage's copies never start, so the
+                // consumers' wait for it runs out (nothing is in flight to drain)
+                if (p.skip_first_stage && it == 0) return true;
                 const uint32_t bytes = static_cast<uint32_t>(count * C::RB);
                 mbar_expect_tx(FULL(slot), 2 * bytes);
                 const size_t off = ((static_cast<size_t>(s.b) * p.Hkv + s.kvh) * S + row) * HD;
@@ -364,7 +370,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
         const int slot = it % C::NS;
         const uint32_t ph = (it / C::NS) & 1;
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(FULL(slot), ph, abort_flag, p.status, DEC_TIMEOUT_NS)))
+                        mbar_wait(FULL(slot), ph, abort_flag, p.status, p.wait_ns)))
             return false;
 #pragma unroll 1
         for (int gi = 0; gi < DEC_GPW; ++gi) {
@@ -499,7 +505,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
         __syncwarp();
         if (lane == 0) mbar_arrive(SYNC(which));
         return __all_sync(0xffffffffu, mbar_wait(SYNC(which), nflush & 1, abort_flag, p.status,
-                                                 DEC_TIMEOUT_NS));
+                                                 p.wait_ns));
     };
 
     auto on_end = [&](const Seg &s) {
@@ -613,9 +619,7 @@ int launch_decode_t(const void *q, const void *Kc, const void *Vc, const DecodeP
                     cudaStream_t stream)
 {
     using C = DecCfg<T, HD, G>;
-    static cudaError_t attr = cudaFuncSetAttribute(
-        swa_decode_split<T, HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
-    if (attr != cudaSuccess) return SWA_ERR_CUDA;
+    if (smem_opt_in<swa_decode_split<T, HD, G>>(C::BYTES) != cudaSuccess) return SWA_ERR_CUDA;
     swa_decode_split<T, HD, G><<<p.P, DEC_THREADS, C::BYTES, stream>>>(
         static_cast<const T *>(q), static_cast<const T *>(Kc), static_cast<const T *>(Vc), p);
     if (cudaGetLastError() != cudaSuccess) return SWA_ERR_CUDA;
@@ -664,7 +668,9 @@ __global__ void swa_cache_append_k(T *__restrict__ Kc, T *__restrict__ Vc,
         const size_t bk = row / T_new;
         const int b = static_cast<int>(bk / Hkv);
         const int p0 = pos0[b];
-        if (p0 < 0) {  // invalid: write nothing, report it
+        // invalid: a negative start, or one whose last position p0+T_new-1
+        // passes INT32_MAX; write nothing and report it
+        if (p0 < 0 || p0 > INT32_MAX - T_new) {
             if (c == 0 && t == 0) atomicOr(status, DEV_ERR_BAD_POS);
             continue;
         }
@@ -753,6 +759,8 @@ int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *
     p.O = O;
     p.lse = lse;
     p.sink = sink;
+    p.wait_ns = DEC_TIMEOUT_NS;
+    p.skip_first_stage = take_injected_stall(SWA_STALL_DECODE, &p.wait_ns) ? 1 : 0;
     const int G = H / Hkv;
     if (dt == SWA_BF16) {
         if (d == 128) return dispatch_g<__nv_bfloat16, 128>(q, Kc, Vc, p, G, stream);

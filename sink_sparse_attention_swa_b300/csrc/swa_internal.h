@@ -2,6 +2,7 @@
 // Not part of the public ABI (that is include/swa.h).
 #pragma once
 
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -191,6 +192,34 @@ enum : int { DEV_ERR_TIMEOUT = 1, DEV_ERR_BAD_POS = 2 };
 
 int *status_ptr();          // device address of the current device's status word
 int read_and_clear_status(cudaStream_t stream);
+
+// A stall injected by swa_debug_inject_stall for the next launch of one kind
+// on the current device: returns true (once) and sets *wait_ns to the wait
+// limit that launch must use; false (and *wait_ns untouched) otherwise.
+bool take_injected_stall(int kind, uint64_t *wait_ns);
+int set_injected_stall(int kind, int64_t wait_ns);
+
+// ---------------------------------------------------------------------------
+// Opt-in to more than 48 KB of dynamic shared memory for one kernel.  The
+// attribute belongs to the current device, so it is set once per (kernel,
+// device): a process that calls the library on several GPUs sets it on each.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+int current_device();  // the current device, or -1 if none (or beyond kMaxDevices)
+#ifdef __CUDACC__
+template <auto Kernel>
+cudaError_t smem_opt_in(int bytes)
+{
+    static std::atomic<int> done[kMaxDevices];  // static storage: starts at zero
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[dev].store(bytes, std::memory_order_release);
+    return e;
+}
+#endif
 
 // ---------------------------------------------------------------------------
 // Launchers (each validates nothing: the public entry points do that).

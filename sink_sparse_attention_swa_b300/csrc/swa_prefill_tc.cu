@@ -111,6 +111,8 @@ struct PrefillParams {
     float *lse;
     const float *sink;  // per-head sink logits [H] or null
     int *status;
+    uint64_t wait_ns;   // limit of every bounded wait of the roles (2 s unless a test sets it)
+    int skip_first_kv;  // test injection: the first key/value copy is left out (see swa.h)
 };
 
 // Work order of both kernels.  Items are ranked by q tile, the last q tile
@@ -213,9 +215,9 @@ __device__ __forceinline__ float ex2(float x)
 
 // All 32 lanes wait; the outcome is made warp-uniform.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          int *status)
+                                          int *status, uint64_t limit_ns)
 {
-    const bool ok = mbar_wait(bar, parity, abort, status, TIMEOUT_NS);
+    const bool ok = mbar_wait(bar, parity, abort, status, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int h = kvh * p.G + hg;
                 const int qb = idx & 1;
                 if (!mbar_wait(BAR(L::Q_EMPTY + qb), ((idx >> 1) & 1) ^ 1, abort_flag, p.status,
-                               TIMEOUT_NS))
+                               p.wait_ns))
                     return false;
                 mbar_expect_tx(BAR(L::Q_FULL + qb), L::QB);
                 const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
                     if (!mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status,
-                                   TIMEOUT_NS)) {
+                                   p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -396,6 +398,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // landmark tiles: class 0 of the stride-rl view; others: this class
                     const int kc = kt.land ? 0 : cls;
                     const bool hi = !PAT || kt.land || cls < p.rem;
+                    // test injection: this stage's copies never start, so the MMA
+                    // warp's wait for them runs out (nothing is in flight to drain)
+                    if (p.skip_first_kv && kv_iter == 0) continue;
                     mbar_expect_tx(BAR(L::K_FULL + st), L::KB);
                     for (int c = 0; c < HD / 64; ++c)
                         load_rows<PAT>(sK + st * L::KB + c * (BN * 128), hi ? &tmK : &tmK2,
@@ -443,12 +448,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bool prev_first = false;
             auto issue_pv = [&]() -> bool {
                 const int pb = prev_c & 1;
-                if (!warp_wait(BAR(L::P_FULL + pb), (prev_c >> 1) & 1, abort_flag, p.status))
+                if (!warp_wait(BAR(L::P_FULL + pb), (prev_c >> 1) & 1, abort_flag, p.status, p.wait_ns))
                     return false;
-                if (!warp_wait(BAR(L::V_FULL + prev_st), prev_ph, abort_flag, p.status))
+                if (!warp_wait(BAR(L::V_FULL + prev_st), prev_ph, abort_flag, p.status, p.wait_ns))
                     return false;
                 if (prev_first &&
-                    !warp_wait(BAR(L::O_EMPTY), (prev_it & 1) ^ 1, abort_flag, p.status))
+                    !warp_wait(BAR(L::O_EMPTY), (prev_it & 1) ^ 1, abort_flag, p.status, p.wait_ns))
                     return false;
                 tc_fence_after();
                 const uint64_t vb = smem_desc_sw128(sV + prev_st * L::KB, BN * 128, 1024);
@@ -468,7 +473,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 int off;
                 const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
                 const int qb = it & 1;
-                if (!warp_wait(BAR(L::Q_FULL + qb), (it >> 1) & 1, abort_flag, p.status)) {
+                if (!warp_wait(BAR(L::Q_FULL + qb), (it >> 1) & 1, abort_flag, p.status, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -476,9 +481,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
                     const int sbuf = c & 1;
-                    if (!warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status) ||
+                    if (!warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, p.wait_ns) ||
                         !warp_wait(BAR(L::S_EMPTY + sbuf), ((c >> 1) & 1) ^ 1, abort_flag,
-                                   p.status)) {
+                                   p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -509,7 +514,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (ok && have_prev) issue_pv();
             // drain: every MMA this warp issued has completed before exit
             tc_commit_e(BAR(L::DRAIN));
-            warp_wait(BAR(L::DRAIN), 0, nullptr, nullptr);
+            warp_wait(BAR(L::DRAIN), 0, nullptr, nullptr, TIMEOUT_NS);
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -532,7 +537,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < tr.count; ++j, ++c) {
                 const int sbuf = c & 1;
-                if (!warp_wait(BAR(L::S_FULL + sbuf), (c >> 1) & 1, abort_flag, p.status)) {
+                if (!warp_wait(BAR(L::S_FULL + sbuf), (c >> 1) & 1, abort_flag, p.status, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -601,7 +606,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         // O must be complete: wait for the previous tile's P V
                         const int pc = c - 1;
                         if (!warp_wait(BAR(L::PV_DONE + (pc & 1)), (pc >> 1) & 1, abort_flag,
-                                       p.status)) {
+                                       p.status, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -641,7 +646,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 l += (l0 + l1) + (l2 + l3);
                 // P buffer (c & 1) is free once the P V of tile c-2 has completed
                 if (c >= 2 && !warp_wait(BAR(L::PV_DONE + (c & 1)), ((c >> 1) & 1) ^ 1, abort_flag,
-                                         p.status)) {
+                                         p.status, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -657,7 +662,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
             const int pc = c - 1;
-            if (!warp_wait(BAR(L::PV_DONE + (pc & 1)), (pc >> 1) & 1, abort_flag, p.status)) {
+            if (!warp_wait(BAR(L::PV_DONE + (pc & 1)), (pc >> 1) & 1, abort_flag, p.status, p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -886,7 +891,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
                 for (int x = 0; x < 2 && ok; ++x) {
                     if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
-                                   TIMEOUT_NS)) {
+                                   p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -902,7 +907,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
                     if (!mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status,
-                                   TIMEOUT_NS)) {
+                                   p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -911,6 +916,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     // landmark tiles: class 0 of the stride-rl view; others: this class
                     const int kc = kt.land ? 0 : cls;
                     const bool hi = !PAT || kt.land || cls < p.rem;
+                    // test injection: this stage's copies never start, so the MMA
+                    // warp's wait for them runs out (nothing is in flight to drain)
+                    if (p.skip_first_kv && kv_iter == 0) continue;
                     // K and V of a stage complete one barrier: the MMA issuer waits
                     // once per key tile
                     mbar_expect_tx(BAR(L::K_FULL + st), 2 * L::KB);
@@ -958,7 +966,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 asm volatile("bar.sync %0, %1;" ::"n"(1 + x), "n"(P_BAR_THREADS) : "memory");
                 if (*abort_flag) return false;
                 if (prev_first && !warp_wait(BAR(L::O_EMPTY + x), (prev_it & 1) ^ 1, abort_flag,
-                                             p.status))
+                                             p.status, p.wait_ns))
                     return false;
                 tc_fence_after();
                 const uint64_t vb = smem_desc_sw128(sV + prev_st * L::KB, BN * 128, 1024);
@@ -1004,8 +1012,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         ok = false;
                         break;
                     }
-                    if ((j == 0 && !warp_wait(BAR(L::Q_FULL + 0), it & 1, abort_flag, p.status)) ||
-                        !warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status)) {
+                    if ((j == 0 && !warp_wait(BAR(L::Q_FULL + 0), it & 1, abort_flag, p.status, p.wait_ns)) ||
+                        !warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -1016,7 +1024,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         ok = false;
                         break;
                     }
-                    if (j == 0 && !warp_wait(BAR(L::Q_FULL + 1), it & 1, abort_flag, p.status)) {
+                    if (j == 0 && !warp_wait(BAR(L::Q_FULL + 1), it & 1, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -1035,7 +1043,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             }
             // drain: every MMA this warp issued has completed before exit
             tc_commit_e(BAR(L::DRAIN));
-            warp_wait(BAR(L::DRAIN), 0, nullptr, nullptr);
+            warp_wait(BAR(L::DRAIN), 0, nullptr, nullptr, TIMEOUT_NS);
         }
     }
     } else {
@@ -1084,7 +1092,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             const int llo = PAT && p.rl > 0 ? land_lo(p.g, p.rl) : 0;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < tr.count; ++j, ++c) {
-                if (!warp_wait(BAR(L::S_FULL + x), c & 1, abort_flag, p.status)) {
+                if (!warp_wait(BAR(L::S_FULL + x), c & 1, abort_flag, p.status, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -1194,7 +1202,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             __nv_bfloat16 *orow = p.O + orow_i * HD;
             const int t_next = pair_item_rank(blockIdx.x, it + 1);
             if (t_next < pairs_per_item_count) load_item(t_next, nxt);
-            if (!warp_wait(BAR(L::O_FULL + x), it & 1, abort_flag, p.status)) {
+            if (!warp_wait(BAR(L::O_FULL + x), it & 1, abort_flag, p.status, p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -1379,19 +1387,6 @@ bool make_view(CUtensorMap *m, const void *base, uint64_t d, uint64_t R, uint64_
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Opt in to a kernel's dynamic shared memory once (one flag per kernel: the
-// kernel itself is the template argument).
-template <auto Kernel>
-cudaError_t set_smem_once(uint32_t bytes)
-{
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [&] {
-        err = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    });
-    return err;
-}
-
 template <int HD, bool PAT>
 int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                    const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
@@ -1400,7 +1395,7 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
     using L2 = Layout2<HD>;
     if (p.G % 2 == 0) {
         // two heads of a GQA pair per work item
-        if (set_smem_once<swa_prefill_bf16_pair_sm103<HD, PAT, false>>(L2::DYN_SMEM) !=
+        if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, PAT, false>>(L2::DYN_SMEM) !=
             cudaSuccess)
             return SWA_ERR_CUDA;
         p.num_items = p.B * p.Hkv * (p.G / 2) * per_unit;
@@ -1412,7 +1407,7 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
     if constexpr (!PAT) {
         // an odd group: two adjacent q tiles of one head per work item (the
         // fixed patterns keep the single-head kernel below)
-        if (set_smem_once<swa_prefill_bf16_pair_sm103<HD, false, true>>(L2::DYN_SMEM) !=
+        if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, false, true>>(L2::DYN_SMEM) !=
             cudaSuccess)
             return SWA_ERR_CUDA;
         p.n_qt = (p.n + 2 * BM - 1) / (2 * BM);  // levels of q-tile pairs
@@ -1423,7 +1418,7 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
         return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
     }
     using L = Layout<HD>;
-    if (set_smem_once<swa_prefill_bf16_sm103<HD, PAT>>(L::DYN_SMEM) != cudaSuccess)
+    if (smem_opt_in<swa_prefill_bf16_sm103<HD, PAT>>(L::DYN_SMEM) != cudaSuccess)
         return SWA_ERR_CUDA;
     p.num_items = p.B * p.H * per_unit;
     const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
@@ -1500,6 +1495,8 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     p.sink = sink;
     p.status = status_ptr();
     if (p.status == nullptr) return SWA_ERR_CUDA;
+    p.wait_ns = TIMEOUT_NS;
+    p.skip_first_kv = take_injected_stall(SWA_STALL_PREFILL, &p.wait_ns) ? 1 : 0;
     if (pat) return launch_kernels<HD, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream);
     return launch_kernels<HD, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream);
 }

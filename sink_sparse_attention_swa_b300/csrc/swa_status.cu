@@ -11,10 +11,37 @@ namespace swa {
 __device__ int g_swa_device_status;
 
 namespace {
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int *g_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
+// one-shot stall injection per device (swa_debug_inject_stall): the kind of
+// launch it applies to (0 = none) and that launch's wait limit
+int g_stall_kind[kMaxDevices] = {};
+uint64_t g_stall_ns[kMaxDevices] = {};
+}  // namespace
+
+bool take_injected_stall(int kind, uint64_t *wait_ns)
+{
+    const int dev = current_device();
+    if (dev < 0) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_stall_kind[dev] != kind) return false;
+    g_stall_kind[dev] = 0;
+    *wait_ns = g_stall_ns[dev];
+    return true;
+}
+
+int set_injected_stall(int kind, int64_t wait_ns)
+{
+    if (kind != 0 && kind != SWA_STALL_PREFILL && kind != SWA_STALL_DECODE) return SWA_ERR_INVALID_ARG;
+    if (kind != 0 && (wait_ns < 100000 || wait_ns > 2000000000)) return SWA_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0) return SWA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_stall_kind[dev] = kind;
+    g_stall_ns[dev] = kind != 0 ? static_cast<uint64_t>(wait_ns) : 0;
+    return SWA_OK;
+}
 
 int current_device()
 {
@@ -22,7 +49,6 @@ int current_device()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
     return dev;
 }
-}  // namespace
 
 int *status_ptr()
 {
