@@ -8,7 +8,12 @@ TFLOP/s (4 * connections * d * B * H floating-point operations; masked or
 padded tile work is not counted).  The decode half of the metric is measured
 in the same run on the streaming-decode workload (B=32, H=32, Hkv=8, d=128,
 w=4096, g=4, pos=100000): one cache append plus one decode per step, reported
-as HBM GB/s over the algorithmic bytes (each cached K/V row read once).
+as HBM GB/s over the algorithmic bytes (each cached K/V row read once).  The
+other three configurations of the method are timed in the same run and
+reported under "configs", each with its own roofline, clocks and CPU-oracle
+baseline: the Gemma-3-like local layer (B=2, H=32, Hkv=16, n=32768, w=1024),
+the long-context layer with sinks (B=1, H=32, Hkv=8, n=131072, w=4096, g=4)
+and the tiny fp32 case (n=512, w=64, d=64, the CUDA-core fp32 kernel).
 
 Timing: W warm-up steps, then K timed steps; L2 is flushed (a 256 MiB write,
 then a 256 MiB read, so the flush's dirty lines are written back before the
@@ -280,8 +285,8 @@ def cpu_oracle_sample(min_seconds=10.0, max_seconds=30.0, seed=0, c=None):
     key = (tuple(sorted(c.items())), seed)
     if key not in _CPU_INPUTS:
         x = synthetic.prefill_inputs(c["B"], c["H"], c["Hkv"], c["n"], c["d"], c["w"], c["g"],
-                                     dtype="bf16", seed=seed, sink_scale=c["sink_scale"],
-                                     device="cpu")
+                                     dtype=c.get("dtype", "bf16"), seed=seed,
+                                     sink_scale=c["sink_scale"], device="cpu")
         _CPU_INPUTS[key] = (x, x.K.double().numpy(), x.V.double().numpy())
     x, K, V = _CPU_INPUTS[key]
     rows_all = synthetic.sample_rows(c["B"], c["H"], c["n"], min(1 << 20, c["B"] * c["H"] * c["n"]),
@@ -391,6 +396,60 @@ def pipelined_e2e(host_in, host_out_like, compute, steps, warmup, stream, dev):
     return start.elapsed_time(end) / steps
 
 
+# the configurations reported under "configs" in the default line, besides
+# the headline prefill (value) and the decode leg
+CONFIG_LEGS = ["gemma3_local_prefill", "long_sink_prefill", "tiny_fp32_prefill"]
+TINY = dict(B=1, H=1, Hkv=1, n=512, d=64, w=64, g=0, sink_scale=1.0, dtype="f32")
+
+
+def config_leg(name, args, swa, synthetic, world, rank, local, dev, stream, flush, pk):
+    """One more configuration of the default run: K timed launches (L2 flushed
+    before each), its clocks, roofline and a CPU-oracle baseline on sampled
+    rows (rank 0, single process)."""
+    c = TINY if name == "tiny_fp32_prefill" else PREFILL_WORKLOADS[name]
+    dtype = c.get("dtype", "bf16")
+    x = synthetic.prefill_inputs(c["B"], c["H"], c["Hkv"], c["n"], c["d"], c["w"], c["g"],
+                                 dtype=dtype, seed=rank, sink_scale=c["sink_scale"], device=dev)
+    out = torch.empty_like(x.Q)
+    fn = lambda: swa.prefill(x.Q, x.K, x.V, c["w"], c["g"], x.scale, out=out, stream=stream)
+    flops = prefill_flops(c)
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        times = time_launches(fn, args.steps, args.warmup, flush, stream)
+    barrier(world)
+    assert swa.device_status(stream) == 0, "device status reported an error"
+    launch_ms = float(np.mean(times))
+    ms = max_over_ranks(launch_ms, world, dev)
+    del x, out
+    torch.cuda.empty_cache()
+    leg = {"workload": name, **{k: v for k, v in c.items() if k != "sink_scale"},
+           "sink_scale": c["sink_scale"], "dtype": dtype, "steps": args.steps,
+           "ms_per_launch": ms, "unit": "TFLOP/s",
+           "value": flops * world / (ms * 1e-3) / 1e12, "useful_flops_per_launch": flops,
+           "clocks": clk.summary(), "gpu_launches": args.steps}
+    if dtype == "bf16":
+        kernel = ("swa_prefill_bf16_pair_sm103" if (c["H"] // c["Hkv"]) % 2 == 0
+                  else "swa_prefill_bf16_sm103")
+        leg["roofline"] = prefill_roofline(c, flops, launch_ms, pk,
+                                           recorded_traffic(kernel, name, PREFILL_KERNEL_SRC),
+                                           kernel)
+    else:
+        leg["roofline"] = None
+        leg["note"] = ("the fp32 CUDA-core path, kept for exactness (max-abs 1e-5 against the "
+                       "oracle); a latency-bound correctness case, not measured against a roofline")
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs = min(args.cpu_seconds, 4.0)
+        tfl, rows, s, thr = cpu_oracle_sample(secs, 3 * secs, c=c)
+        _CPU_INPUTS.clear()  # host copies of this configuration's inputs
+        leg["cpu_baseline"] = {
+            "value": tfl, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "sample": f"{rows} query rows of {name} (uniformly sampled over heads and "
+                      f"positions), fp64, {s:.1f} s; a whole launch would take "
+                      f"{flops / (tfl * 1e12):.1f} s (extrapolated from the rows)"}
+    return leg
+
+
 def run_swa(args):
     import sink_sparse_attention_swa_b300 as swa
     from sink_sparse_attention_swa_b300 import synthetic
@@ -471,6 +530,11 @@ def run_swa(args):
     if args.only in ("all", "decode"):
         decode_line = decode_leg(args, swa, synthetic, world, rank, local, dev, stream, flush, pk)
 
+    configs = None
+    if args.only == "all" and not args.no_configs and args.workload == "mistral_like_prefill":
+        configs = {nm: config_leg(nm, args, swa, synthetic, world, rank, local, dev, stream,
+                                  flush, pk) for nm in CONFIG_LEGS}
+
     cpu = None
     if (rank == 0 and world == 1 and not args.no_cpu_baseline
             and args.only in ("all", "prefill")):
@@ -499,11 +563,14 @@ def run_swa(args):
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "clocks": clk_summary,
         "e2e": e2e,
-        "gpu_launches": args.steps if value is not None else 0,
+        "gpu_launches": ((args.steps if value is not None else 0)
+                         + (decode_line["gpu_launches"] if decode_line else 0)
+                         + sum(v["gpu_launches"] for v in (configs or {}).values())),
         "roofline": None if value is None else prefill_roofline(c, flops, launch_ms, pk,
                                                                 traffic, kernel),
         "cpu_baseline": cpu,
         "decode": decode_line,
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
 
@@ -695,6 +762,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations (Gemma-3-like, long-context, tiny fp32)")
     ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "chunk"])
     ap.add_argument("--workload", default="mistral_like_prefill", choices=sorted(PREFILL_WORKLOADS))
     args = ap.parse_args()

@@ -195,7 +195,9 @@ int swa_prefill_chunk(const void *Q, const void *k_new, const void *v_new, void 
  * not yet written (pos < w-1) and sink slots of positions still inside the
  * window are not read.
  *   q [B][H][d], Kcache, Vcache [B][Hkv][w+g][d], O [B][H][d]: bf16, device.
- *   The group size H/Hkv is 1, 2, 4 or 8 (SWA_ERR_UNSUPPORTED otherwise).
+ *   Any group size G = H/Hkv: the kernels score up to 8 heads of a group per
+ *   pass over the cache rows; a larger group is split into ceil(G/8) equal
+ *   sub-groups that stream the same rows side by side.
  * Split-K over the cached keys, then a log-sum-exp merge: a first kernel cuts
  * the cache rows of all (sequence, kv head) pairs, laid end to end, into equal
  * contiguous shares, one per CTA of a single resident wave, and writes one

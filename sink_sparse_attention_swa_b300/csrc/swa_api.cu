@@ -224,7 +224,7 @@ int swa_prefill(const void *Q, const void *K, const void *V, void *O, int B, int
 size_t swa_decode_workspace_bytes(int B, int H, int Hkv, int d, int w, int g, int num_splits)
 {
     if (check_heads(B, H, Hkv, d, w, g) != SWA_OK || num_splits < 0 || num_splits > 1024) return 0;
-    return decode_workspace_bytes(B, H, Hkv, d, decode_ctas(B, Hkv, w, g, num_splits));
+    return decode_workspace_bytes(B, H, Hkv, d, decode_ctas(B, H, Hkv, w, g, num_splits));
 }
 
 int swa_decode_sink_logit(const void *q, const void *Kcache, const void *Vcache,
@@ -235,8 +235,6 @@ int swa_decode_sink_logit(const void *q, const void *Kcache, const void *Vcache,
 {
     int rc = check_heads(B, H, Hkv, d, w, g);
     if (rc != SWA_OK) return rc;
-    const int G = H / Hkv;
-    if (G != 1 && G != 2 && G != 4 && G != 8) return SWA_ERR_UNSUPPORTED;
     if (dtype != SWA_BF16 && dtype != SWA_F32) return SWA_ERR_INVALID_ARG;
     if (!scale_ok(scale) || num_splits < 0 || num_splits > 1024) return SWA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(Kcache) || !aligned16(Vcache) || !aligned16(O) ||
@@ -245,7 +243,7 @@ int swa_decode_sink_logit(const void *q, const void *Kcache, const void *Vcache,
     if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
     if (sink_logit != nullptr && (reinterpret_cast<uintptr_t>(sink_logit) & 3u))
         return SWA_ERR_INVALID_ARG;
-    const int ctas = decode_ctas(B, Hkv, w, g, num_splits);
+    const int ctas = decode_ctas(B, H, Hkv, w, g, num_splits);
     const size_t need = decode_workspace_bytes(B, H, Hkv, d, ctas);
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
         return SWA_ERR_WORKSPACE;
@@ -267,7 +265,7 @@ int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int3
 {
     int rc = check_heads(B, H, Hkv, d, w, g);
     if (rc != SWA_OK) return rc;
-    const size_t need = decode_workspace_bytes(B, H, Hkv, d, decode_ctas(B, Hkv, w, g, 0));
+    const size_t need = decode_workspace_bytes(B, H, Hkv, d, decode_ctas(B, H, Hkv, w, g, 0));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the lock is held until both kernels are enqueued, so the table is never
     // changed under a call that is still choosing its buffer

@@ -151,12 +151,15 @@ struct DecCfg {
 
 struct DecodeParams {
     int B, H, Hkv, w, g;
+    int G;          // query heads per kv head
+    int nsub, Gs;   // sub-groups per kv head and real heads per sub-group (decode_groups)
+    int Hv;         // virtual kv heads, Hkv * nsub: one segment per (sequence, virtual head)
     int P;          // CTAs of the split pass
-    long long T;    // B * Hkv * (w + g) slots, laid end to end
+    long long T;    // B * Hv * (w + g) slots, laid end to end
     float sl2;      // scale * log2(e)
     const int32_t *pos;
     int *status;    // device status word (a negative position is reported there)
-    float *ws;      // partials [P + B*Hkv][G][HD + 2]: m, l, o
+    float *ws;      // partials [P + B*Hv][Gp][HD + 2]: m, l, o
     void *O;        // [B][H][d]
     float *lse;     // [B][H] or null
     const float *sink;  // per-head sink logits [H] or null
@@ -179,6 +182,8 @@ __device__ __forceinline__ int cta_of(long long T, int P, long long x)
 
 struct Seg {
     int b, kvh, bk;
+    int h0;      // the first query head of the segment's sub-group
+    int nh;      // its real heads (the rest, up to the group width, are padding)
     int ring_lo, ring_hi;  // valid ring rows of this CTA's share of the segment
     int sink_lo, sink_hi;  // valid sink rows (slot numbers w..)
     bool bad_pos;
@@ -188,8 +193,12 @@ __device__ __forceinline__ Seg make_seg(const DecodeParams &p, long long bk, int
 {
     Seg s;
     s.bk = static_cast<int>(bk);
-    s.b = static_cast<int>(bk / p.Hkv);
-    s.kvh = static_cast<int>(bk % p.Hkv);
+    s.b = static_cast<int>(bk / p.Hv);
+    const int v = static_cast<int>(bk % p.Hv);
+    s.kvh = v / p.nsub;
+    const int u = v % p.nsub;
+    s.h0 = s.kvh * p.G + u * p.Gs;
+    s.nh = min(p.Gs, p.G - u * p.Gs);
     // 64-bit: pos may be as large as INT32_MAX
     long long pos = __ldg(p.pos + s.b);
     s.bad_pos = pos < 0;
@@ -345,15 +354,18 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
         if (s.bad_pos && threadIdx.x == 0) atomicOr(p.status, DEV_ERR_BAD_POS);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
-            const T *qr = q + (static_cast<size_t>(s.b) * p.H + s.kvh * G + hh) * HD;
+            // a padding head of the sub-group scores with q = 0 (never written out)
+            const bool real = hh < s.nh;
+            const T *qr = q + (static_cast<size_t>(s.b) * p.H + s.h0 + (real ? hh : 0)) * HD;
 #pragma unroll
             for (int c = 0; c < C::CPL; ++c) {
                 const int chunk = cidx * C::CPL + ((c + rot) % C::CPL);
 #pragma unroll
                 for (int e = 0; e < C::EPC; e += 2)
                     q2[hh][(c * C::EPC + e) / 2] =
-                        pk2(U::to_f(qr[chunk * C::EPC + e]) * p.sl2,
-                            U::to_f(qr[chunk * C::EPC + e + 1]) * p.sl2);
+                        real ? pk2(U::to_f(qr[chunk * C::EPC + e]) * p.sl2,
+                                   U::to_f(qr[chunk * C::EPC + e + 1]) * p.sl2)
+                             : pk2(0.f, 0.f);
             }
             m[hh] = M_EMPTY;
 #pragma unroll
@@ -605,7 +617,9 @@ __global__ void __launch_bounds__(G * HD) swa_decode_merge(const DecodeParams p)
         L += sc * x[1];
         o += sc * x[2 + col];
     }
-    const int b = bk / p.Hkv, h = (bk % p.Hkv) * G + hh;
+    const int b = bk / p.Hv, v = bk % p.Hv, u = v % p.nsub;
+    if (hh >= min(p.Gs, p.G - u * p.Gs)) return;  // a padding head of the sub-group
+    const int h = (v / p.nsub) * p.G + u * p.Gs + hh;
     const size_t bh = static_cast<size_t>(b) * p.H + h;
     float row_lse;
     const float f = L > 0.f ? finish_row(M, L, p.sink, h, &row_lse) : 0.f;
@@ -624,7 +638,7 @@ int launch_decode_t(const void *q, const void *Kc, const void *Vc, const DecodeP
         static_cast<const T *>(q), static_cast<const T *>(Kc), static_cast<const T *>(Vc), p);
     if (cudaGetLastError() != cudaSuccess) return SWA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.Hkv));
+    cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.Hv));
     cfg.blockDim = dim3(G * HD);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -711,13 +725,14 @@ int launch_append_t(void *Kc, void *Vc, const void *kn, const void *vn, const in
 
 }  // namespace
 
-int decode_ctas(int B, int Hkv, int w, int g, int num_splits)
+int decode_ctas(int B, int H, int Hkv, int w, int g, int num_splits)
 {
-    const long long T = static_cast<long long>(B) * Hkv * (static_cast<long long>(w) + g);
+    const long long Hv = static_cast<long long>(Hkv) * decode_groups(H / Hkv).nsub;
+    const long long T = static_cast<long long>(B) * Hv * (static_cast<long long>(w) + g);
     long long P;
     if (num_splits > 0) {
-        // about num_splits CTAs per (sequence, kv head) segment
-        P = static_cast<long long>(num_splits) * B * Hkv;
+        // about num_splits CTAs per (sequence, virtual kv head) segment
+        P = static_cast<long long>(num_splits) * B * Hv;
     } else {
         // one resident wave, each CTA streaming at least MIN_SLOTS_PER_CTA rows
         P = static_cast<long long>(DEC_CTAS_PER_SM) * num_sms();
@@ -732,9 +747,11 @@ int decode_ctas(int B, int Hkv, int w, int g, int num_splits)
 
 size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int ctas)
 {
-    // one partial (m, l, o[d]) per head of the group for every (CTA, segment)
-    // pair that meets: at most ctas + B*Hkv - 1 of them, indexed cta + segment
-    return (static_cast<size_t>(ctas) + static_cast<size_t>(B) * Hkv) * (H / Hkv) *
+    // one partial (m, l, o[d]) per head of the padded sub-group for every
+    // (CTA, segment) pair that meets: at most ctas + B*Hv - 1 of them, indexed
+    // cta + segment
+    const DecodeGroups dg = decode_groups(H / Hkv);
+    return (static_cast<size_t>(ctas) + static_cast<size_t>(B) * Hkv * dg.nsub) * dg.Gp *
            (static_cast<size_t>(d) + 2) * sizeof(float);
 }
 
@@ -749,8 +766,13 @@ int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *
     p.Hkv = Hkv;
     p.w = w;
     p.g = g;
+    const DecodeGroups dg = decode_groups(H / Hkv);
+    p.G = H / Hkv;
+    p.nsub = dg.nsub;
+    p.Gs = dg.Gs;
+    p.Hv = Hkv * dg.nsub;
     p.P = ctas;
-    p.T = static_cast<long long>(B) * Hkv * (static_cast<long long>(w) + g);
+    p.T = static_cast<long long>(B) * p.Hv * (static_cast<long long>(w) + g);
     p.sl2 = scale * 1.4426950408889634f;
     p.pos = pos;
     p.status = status_ptr();
@@ -761,7 +783,7 @@ int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *
     p.sink = sink;
     p.wait_ns = DEC_TIMEOUT_NS;
     p.skip_first_stage = take_injected_stall(SWA_STALL_DECODE, &p.wait_ns) ? 1 : 0;
-    const int G = H / Hkv;
+    const int G = dg.Gp;  // the kernels' group width
     if (dt == SWA_BF16) {
         if (d == 128) return dispatch_g<__nv_bfloat16, 128>(q, Kc, Vc, p, G, stream);
         if (d == 64) return dispatch_g<__nv_bfloat16, 64>(q, Kc, Vc, p, G, stream);

@@ -249,9 +249,28 @@ int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, flo
 int launch_chunk_gather(void *Kx, void *Vx, const void *Kc, const void *Vc, const void *k_new,
                         const void *v_new, const int32_t *pos0, int B, int Hkv, int T, int d,
                         int w, int g, swa_dtype dt, cudaStream_t stream);
+// Decode of any GQA group size G: the G query heads of a kv head are split
+// into nsub = ceil(G / 8) sub-groups of Gs = ceil(G / nsub) heads, each padded
+// to Gp (the next of 1, 2, 4, 8, the group widths the decode kernels are built
+// for) with dummy heads whose results are never written.  A sub-group is a
+// "virtual kv head": Hv = Hkv * nsub of them, sub-group u of kv head k being
+// virtual head k * nsub + u, which reads kv head k's cache and query heads
+// k * G + u * Gs + (0 .. Gs-1).
+struct DecodeGroups {
+    int nsub, Gs, Gp;
+};
+__host__ __device__ inline DecodeGroups decode_groups(int G)
+{
+    DecodeGroups r;
+    r.nsub = (G + 7) / 8;
+    r.Gs = (G + r.nsub - 1) / r.nsub;
+    r.Gp = 1;
+    while (r.Gp < r.Gs) r.Gp <<= 1;
+    return r;
+}
 // CTAs of the decode split pass: num_splits > 0 asks for about that many per
-// (sequence, kv head); 0 picks one resident wave on the current device.
-int decode_ctas(int B, int Hkv, int w, int g, int num_splits);
+// (sequence, virtual kv head); 0 picks one resident wave on the current device.
+int decode_ctas(int B, int H, int Hkv, int w, int g, int num_splits);
 size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int ctas);
 int launch_decode(const void *q, const void *Kc, const void *Vc, const int32_t *pos,
                   const float *sink, int B,

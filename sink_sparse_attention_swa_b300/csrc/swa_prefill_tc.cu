@@ -273,6 +273,60 @@ __device__ __forceinline__ void store_o_rows(uint32_t o_addr, float inv_l,
     }
 }
 
+// The same epilogue in rounds of 32 columns, for a warp with few registers:
+// each round loads 32 columns of O from tensor memory, scales and rounds them,
+// turns them around in `stage` and stores them.  Once the last round's load
+// has completed the warp arrives on `empty_bar` (the O columns may be
+// overwritten), before that round's stores.
+template <int HD>
+__device__ __forceinline__ void store_o_rows_chunked(uint32_t o_addr, float inv_l,
+                                                     __nv_bfloat16 *orow, bool row_ok,
+                                                     uint8_t *stage, int lane, uint32_t empty_bar)
+{
+    const int sub = lane & 3;
+    uint64_t dst[4];
+    bool dok[4];
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+        const int src = st * 8 + (lane >> 2);
+        dst[st] = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(orow), src);
+        dok[st] = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, src) != 0;
+    }
+    uint4 *mine = reinterpret_cast<uint4 *>(stage + lane * STAGE_ROW);
+#pragma unroll 1
+    for (int q = 0; q < HD / 32; ++q) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + q * 32, o);
+        tmem_ld_wait();
+        reg_fence32(o);
+        if (q == HD / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar);
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+            mine[v] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * v]) * inv_l,
+                                             __uint_as_float(o[8 * v + 1]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l,
+                                             __uint_as_float(o[8 * v + 3]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l,
+                                             __uint_as_float(o[8 * v + 5]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l,
+                                             __uint_as_float(o[8 * v + 7]) * inv_l));
+        __syncwarp();
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+            const uint4 val =
+                *reinterpret_cast<const uint4 *>(stage + (st * 8 + (lane >> 2)) * STAGE_ROW + sub * 16);
+            if (dok[st])
+                reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(dst[st]) + q * 32)[sub] =
+                    val;
+        }
+        __syncwarp();
+    }
+}
+
 // Units of the pair kernel per kv head: head pairs of an even group, or single
 // heads whose two halves are two q tiles (odd groups); and the head of half x.
 template <bool QP>
@@ -700,24 +754,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // take turns with the tensor core; the MMA warp issues, per key tile c,
 //     P_A(c-1) V, S_A(c) = Q_A K^T, P_B(c-1) V, S_B(c) = Q_B K^T
 // so softmax A(c) runs while the tensor core computes P_B(c-1) V and S_B(c),
-// and the other way round.  384 threads in three warpgroups: warpgroup 0 holds
-// the TMA warp (0) and the MMA warp (1) and gives registers away (setmaxnreg
-// down to REGS_CTRL), the softmax warpgroups take them (up to REGS_SOFTMAX), so
-// a full 128-column S row stays in registers.  TMEM (512 columns): O_A [0,128),
-// S_A [128,256), O_B [256,384), S_B [384,512); P (bf16) is written back over
-// the first half of its S buffer.  A tcgen05.commit tracks every MMA issued
-// before it, so the S_X(c) barrier also tells softmax X that P_X(c-1) V has
-// landed in O_X and that O_X may be rescaled.  Each softmax warp stages its
-// output rows through STAGE_WARP bytes of shared memory (store_o_rows).
+// and the other way round.  512 threads in four warpgroups: warpgroup 0 holds
+// the TMA warp (0) and the MMA warp (1), warpgroups 1 and 2 run the softmax of
+// the two heads, and warpgroup 3 writes the output.  setmaxnreg moves
+// registers from warpgroups 0 and 3 to the softmax warpgroups (REGS_SOFTMAX),
+// so a full 128-column S row stays in registers.  TMEM (512 columns): O_A
+// [0,128), S_A [128,256), O_B [256,384), S_B [384,512); P (bf16) is written
+// back over the first half of its S buffer.  A tcgen05.commit tracks every MMA
+// issued before it, so the S_X(c) barrier also tells softmax X that P_X(c-1) V
+// has landed in O_X and that O_X may be rescaled.
+// The epilogue warpgroup takes each item's output off the softmax warps'
+// path: after its last tile a softmax warp only leaves the row's normaliser
+// and LSE in shared memory and goes on with the next item; the epilogue warps
+// wait for the item's last P V (O_FULL), read O_X out of tensor memory (each
+// warp its TMEM lane quarter), free it for the next item (O_EMPTY), and store
+// it through STAGE_WARP bytes of shared memory per warp (store_o_rows_chunked).
 // ------------------------------------------------------------------------
-constexpr int NTHREADS2 = 384;
+constexpr int NTHREADS2 = 512;
 // named barriers 1 (head A) and 2 (head B): a softmax warpgroup's 128 threads
 // arrive when P is in tensor memory, the 32 threads of the MMA warp wait
 constexpr int P_BAR_THREADS = 128 + 32;
-// registers per thread after the hand-over: 128 * (104 + 200 + 200) equals the
-// 384 * 168 registers the kernel is launched with
-constexpr int REGS_CTRL = 104;
-constexpr int REGS_SOFTMAX = 200;
+// registers per thread after the hand-over: 128 * (80 + 176 + 176 + 80)
+// equals the 512 * 128 registers the kernel is launched with
+constexpr int REGS_CTRL = 80;
+constexpr int REGS_SOFTMAX = 176;
+constexpr int REGS_EPI = 80;
 
 template <int HD>
 struct Layout2 {
@@ -737,12 +798,15 @@ struct Layout2 {
         P_FULL = S_FULL + 2,
         O_FULL = P_FULL + 2,
         O_EMPTY = O_FULL + 2,
-        DRAIN = O_EMPTY + 2,
+        ROW_STATS = O_EMPTY + 2,  // [head x][item parity]: a row's normaliser and LSE are posted
+        DRAIN = ROW_STATS + 4,
         NBAR = DRAIN + 1
     };
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t STAGE_OFF = (MISC_OFF + 16 + 15) & ~15u;  // 8 softmax warps
-    static constexpr uint32_t BYTES = STAGE_OFF + 8 * STAGE_WARP;
+    // (1/l, lse) per row: [item parity][head x][BM rows] float2
+    static constexpr uint32_t STATS_OFF = (MISC_OFF + 16 + 15) & ~15u;
+    static constexpr uint32_t STAGE_OFF = STATS_OFF + 2 * 2 * BM * 8;  // 4 epilogue warps
+    static constexpr uint32_t BYTES = STAGE_OFF + 4 * STAGE_WARP;
     static constexpr uint32_t DYN_SMEM = (BYTES + 1024 > 120 * 1024) ? BYTES + 1024 : 120 * 1024;
 };
 
@@ -758,6 +822,7 @@ __device__ __forceinline__ int pair_item_rank(int c, int k)
     const int P = static_cast<int>(gridDim.x);
     return k * P + ((k & 1) ? P - 1 - c : c);
 }
+
 
 // Softmax warpgroup x: P_x of the current key tile is in tensor memory.
 __device__ __forceinline__ void p_arrive(int x)
@@ -846,6 +911,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             mbar_init(BAR(L::P_FULL + x), 4);
             mbar_init(BAR(L::O_FULL + x), 1);
             mbar_init(BAR(L::O_EMPTY + x), 4);
+            mbar_init(BAR(L::ROW_STATS + 2 * x), 4);
+            mbar_init(BAR(L::ROW_STATS + 2 * x + 1), 4);
         }
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(BAR(L::K_FULL + i), 1);
@@ -971,11 +1038,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 tc_fence_after();
                 const uint64_t vb = smem_desc_sw128(sV + prev_st * L::KB, BN * 128, 1024);
                 const uint32_t o_t = tmem + x * 256, p_t = tmem + x * 256 + 128;
-                mma_ts_e(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
-#pragma unroll
-                for (int ks = 1; ks < BN / 16; ++ks)
-                    mma_ts_e(o_t, p_t + ks * 8, vb + static_cast<uint64_t>((ks * 16 * 128) >> 4),
-                             idesc_o, 1u);
+                mma_ts_group8(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
                 if (x == 1) tc_commit_e(BAR(L::KV_EMPTY + prev_st));
                 if (prev_last) tc_commit_e(BAR(L::O_FULL + x));
                 return true;
@@ -986,12 +1049,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 const uint64_t qb = smem_desc_sw128(sQ + x * L::QB, 16, 1024);
                 const uint64_t kb = smem_desc_sw128(sK + st * L::KB, 16, 1024);
                 const uint32_t s_t = tmem + x * 256 + 128;
-#pragma unroll
-                for (int ks = 0; ks < HD / 16; ++ks) {
-                    const uint32_t qo = ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4;
-                    const uint32_t ko = ((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4;
-                    mma_ss_e(s_t, qb + qo, kb + ko, idesc_s, ks > 0 ? 1u : 0u);
-                }
+                mma_ss_group<HD / 16>(s_t, qb, kb, idesc_s);
                 tc_commit_e(BAR(L::S_FULL + x));
                 if (last) tc_commit_e(BAR(L::Q_EMPTY + x));
             };
@@ -1046,7 +1104,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             warp_wait(BAR(L::DRAIN), 0, nullptr, nullptr, TIMEOUT_NS);
         }
     }
-    } else {
+    } else if (warp < 12) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));
         // ------------------------------------------------------------ softmax A / B
         const int x = (warp >> 2) - 1;           // 0: head h0 (warps 4-7), 1: h0+1 (warps 8-11)
@@ -1057,6 +1115,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         const uint32_t s_addr = o_addr + 128;
         const float sl2 = p.sl2;
         const uint64_t sl2x2 = pack2(__float_as_uint(sl2), __float_as_uint(sl2));
+        float2 *stats = reinterpret_cast<float2 *>(smem + L::STATS_OFF);
         int c = 0, it = 0;
         bool ok = true;
         // the item's sequence, head, class, query offset and key tiles; the next
@@ -1075,7 +1134,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         int t = pair_item_rank(blockIdx.x, 0);
         if (t < pairs_per_item_count) load_item(t, nxt);
         while (ok && t < pairs_per_item_count) {
-            const int b = nxt.b, h = nxt.h, cls = nxt.cls, off = nxt.off;
+            const int h = nxt.h;
             const TileRange tr = nxt.tr;
             // this half's own rows: with q-tile pairs, half x is q tile 2k + x,
             // and tiles of the walk are classed (full or not) against its rows
@@ -1188,31 +1247,15 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 p_arrive(x);
             }
             if (!ok) break;
-            // ---------------------------------------------------------- epilogue
-            // the row's normaliser and output address, and the next item, while
-            // the last P V of this one is still running
+            // the row's normaliser and LSE to the epilogue warpgroup, which
+            // writes this item's output while this warp goes on with the next
             float row_lse;
             const float inv_l = finish_row(m, l, p.sink, h, &row_lse);
-            // the query row of this thread: its index in the class subsequence,
-            // and its position c + R t
-            const int t_row = i - off;
-            const bool row_ok = t_row < (!PAT ? p.n : cls < p.rem ? p.n_hi : p.n_lo);
-            const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n +
-                                  (PAT ? cls + static_cast<size_t>(p.R) * t_row : t_row);
-            __nv_bfloat16 *orow = p.O + orow_i * HD;
+            stats[((it & 1) * 2 + x) * BM + r] = make_float2(inv_l, row_lse);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(L::ROW_STATS + 2 * x + (it & 1)));
             const int t_next = pair_item_rank(blockIdx.x, it + 1);
             if (t_next < pairs_per_item_count) load_item(t_next, nxt);
-            if (!warp_wait(BAR(L::O_FULL + x), it & 1, abort_flag, p.status, p.wait_ns)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            store_o_rows<HD>(o_addr, inv_l, orow, row_ok,
-                             smem + L::STAGE_OFF + (warp - 4) * STAGE_WARP, lane);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(L::O_EMPTY + x));
-            if (p.lse != nullptr && row_ok) p.lse[orow_i] = row_lse;
             ++it;
             t = t_next;
         }
@@ -1222,6 +1265,46 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             *abort_flag = 1;
             __syncwarp();
             p_arrive(x);
+        }
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
+        // ------------------------------------------------------------ epilogue
+        // Per item and head: wait for the softmax's row statistics and for the
+        // item's last P V, then write O / l as bf16 (and the LSE).
+        const int sub = warp & 3;                // TMEM lane quarter this warp may access
+        const int r = sub * 32 + lane;           // query row within the tile
+        const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
+        const float2 *stats = reinterpret_cast<const float2 *>(smem + L::STATS_OFF);
+        uint8_t *stage = smem + L::STAGE_OFF + sub * STAGE_WARP;
+        int it = 0;
+        bool ok = true;
+        for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
+             t = pair_item_rank(blockIdx.x, ++it)) {
+            int b, hp, kvh, qt, cls, off;
+            decode_level_item<PAT>(t, p, pair_units<QP>(p), b, hp, kvh, qt, cls);
+            const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
+            const int nq = !PAT ? p.n : cls < p.rem ? p.n_hi : p.n_lo;
+#pragma unroll 1
+            for (int x = 0; x < 2; ++x) {
+                if (!warp_wait(BAR(L::ROW_STATS + 2 * x + (it & 1)), (it >> 1) & 1, abort_flag,
+                               p.status, p.wait_ns) ||
+                    !warp_wait(BAR(L::O_FULL + x), it & 1, abort_flag, p.status, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float2 sv = stats[((it & 1) * 2 + x) * BM + r];
+                const int h = pair_head<QP>(p, kvh, hp, x);
+                // this thread's query row: half x of a q-tile pair is q tile 2k + x
+                const int i = tr.q0 + (QP ? x * BM : 0) + r;
+                const int t_row = i - off;
+                const bool row_ok = t_row < nq;
+                const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n +
+                                      (PAT ? cls + static_cast<size_t>(p.R) * t_row : t_row);
+                store_o_rows_chunked<HD>(tmem + lane_off + x * 256, sv.x, p.O + orow_i * HD,
+                                         row_ok, stage, lane, BAR(L::O_EMPTY + x));
+                if (p.lse != nullptr && row_ok) p.lse[orow_i] = sv.y;
+            }
         }
     }
 #undef BAR

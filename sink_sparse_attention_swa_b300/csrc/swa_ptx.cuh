@@ -227,6 +227,65 @@ __device__ __forceinline__ void tc_commit_e(uint32_t bar)
         : "memory");
 }
 
+// Grouped issue: one asm block elects a lane once and issues a whole K-loop
+// of MMAs, with the k-step offsets added to the low word of each shared-memory
+// descriptor (the start-address field; these offsets never carry out of it).
+// One instruction stream with independent adds keeps the issuing warp short.
+// S = A * B^T over K = 16*NK with both operands K-major in 128-byte swizzled
+// 64-column chunks of 128 rows (16 KB apart): k-step ks adds
+// ((ks>>2)*16384 + (ks&3)*32) >> 4 to both descriptors' start address.
+template <int NK>
+__device__ __forceinline__ void mma_ss_group(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc)
+{
+    const uint32_t al = static_cast<uint32_t>(a), ah = static_cast<uint32_t>(a >> 32);
+    const uint32_t bl = static_cast<uint32_t>(b), bh = static_cast<uint32_t>(b >> 32);
+#define SWA_MMA_SS(OFF) \
+    "add.u32 xl, %1, " #OFF ";\n\tadd.u32 yl, %3, " #OFF ";\n\t" \
+    "mov.b64 xd, {xl, %2};\n\tmov.b64 yd, {yl, %4};\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], xd, yd, %5, t;\n\t"
+    if constexpr (NK == 8) {
+        asm volatile("{\n\t.reg .pred e, f, t;\n\t.reg .b32 xl, yl;\n\t.reg .b64 xd, yd;\n\t"
+                     "elect.sync _|e, 0xffffffff;\n\t"
+                     "setp.ne.b32 f, %5, %5;\n\tsetp.eq.b32 t, %5, %5;\n\t"
+                     "mov.b64 xd, {%1, %2};\n\tmov.b64 yd, {%3, %4};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], xd, yd, %5, f;\n\t"
+                     SWA_MMA_SS(2) SWA_MMA_SS(4) SWA_MMA_SS(6) SWA_MMA_SS(1024) SWA_MMA_SS(1026)
+                     SWA_MMA_SS(1028) SWA_MMA_SS(1030) "}\n" ::"r"(d),
+                     "r"(al), "r"(ah), "r"(bl), "r"(bh), "r"(idesc)
+                     : "memory");
+    } else {
+        asm volatile("{\n\t.reg .pred e, f, t;\n\t.reg .b32 xl, yl;\n\t.reg .b64 xd, yd;\n\t"
+                     "elect.sync _|e, 0xffffffff;\n\t"
+                     "setp.ne.b32 f, %5, %5;\n\tsetp.eq.b32 t, %5, %5;\n\t"
+                     "mov.b64 xd, {%1, %2};\n\tmov.b64 yd, {%3, %4};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], xd, yd, %5, f;\n\t"
+                     SWA_MMA_SS(2) SWA_MMA_SS(4) SWA_MMA_SS(6) "}\n" ::"r"(d),
+                     "r"(al), "r"(ah), "r"(bl), "r"(bh), "r"(idesc)
+                     : "memory");
+    }
+#undef SWA_MMA_SS
+}
+// O (+)= P * V over K = 128 keys: P in tensor memory (8 columns per k-step),
+// V N-major in shared memory (k-step ks adds ks*16 rows * 128 B >> 4 = 128).
+__device__ __forceinline__ void mma_ts_group8(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                              uint32_t acc0)
+{
+    const uint32_t bl = static_cast<uint32_t>(b), bh = static_cast<uint32_t>(b >> 32);
+#define SWA_MMA_TS(AO, BO) \
+    "add.u32 ta, %1, " #AO ";\n\tadd.u32 yl, %2, " #BO ";\n\tmov.b64 yd, {yl, %3};\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yd, %4, t;\n\t"
+    asm volatile("{\n\t.reg .pred e, f, t;\n\t.reg .b32 ta, yl;\n\t.reg .b64 yd;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "setp.ne.b32 f, %5, 0;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+                 "mov.b64 yd, {%2, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], yd, %4, f;\n\t"
+                 SWA_MMA_TS(8, 128) SWA_MMA_TS(16, 256) SWA_MMA_TS(24, 384) SWA_MMA_TS(32, 512)
+                 SWA_MMA_TS(40, 640) SWA_MMA_TS(48, 768) SWA_MMA_TS(56, 896) "}\n" ::"r"(d),
+                 "r"(a_tmem), "r"(bl), "r"(bh), "r"(idesc), "r"(acc0)
+                 : "memory");
+#undef SWA_MMA_TS
+}
+
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major,
 // B K-major (b_mn_major = 0) or N-major (1), shape M x N.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,

@@ -100,9 +100,10 @@ def test_host_validation_rejects_before_launch(swa):
                             None) == -1  # misaligned Q
     assert L.swa_prefill_ex(None, FAKE, FAKE, FAKE, None, 1, 4, 2, 16, 128, 4, 0, 0.1, 0,
                             None) == -1  # null Q
-    # decode: GQA group of 3 unsupported, bad split count, missing workspace
+    # decode: any group size is accepted (a group of 3 here; the missing
+    # workspace is what is refused), bad split count, missing workspace
     assert L.swa_decode_ex(FAKE, FAKE, FAKE, FAKE, 1, 6, 2, 128, 8, 0, 0.1, FAKE, None, 0, 0,
-                           None, 0, None) == -2
+                           None, 0, None) == -6
     assert L.swa_decode_ex(FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 128, 8, 0, 0.1, FAKE, None, 0, 2000,
                            None, 0, None) == -1
     assert L.swa_decode_ex(FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 128, 8, 0, 0.1, FAKE, None, 0, 4,
@@ -113,6 +114,12 @@ def test_host_validation_rejects_before_launch(swa):
     assert L.swa_decode_workspace_bytes(2, 4, 2, 128, 8, 0, 1) == (4 + 4) * 2 * 130 * 4
     # more CTAs than cache rows are not used: at most one row per CTA
     assert L.swa_decode_workspace_bytes(1, 2, 1, 64, 3, 1, 1000) == (4 + 1) * 2 * 66 * 4
+    # a group of 3 is scored as a padded group of 4
+    assert L.swa_decode_workspace_bytes(2, 6, 2, 128, 8, 0, 4) == (16 + 4) * 4 * 130 * 4
+    # a group of 16 is two sub-groups of 8: B * Hkv * 2 segments
+    assert L.swa_decode_workspace_bytes(2, 16, 1, 128, 8, 0, 1) == (4 + 4) * 8 * 130 * 4
+    # a group of 12 is two sub-groups of 6, each padded to 8
+    assert L.swa_decode_workspace_bytes(1, 12, 1, 64, 8, 0, 2) == (4 + 2) * 8 * 66 * 4
     # append: negative T, misaligned cache; T == 0 is a no-op
     assert L.swa_cache_append(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 1, 2, 128, 8, 0, 0, None) == -1
     assert L.swa_cache_append(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 1, 1, 2, 128, 8, 0, 0, None) == -1

@@ -128,8 +128,56 @@ def test_negative_position_is_reported(swa):
     assert swa.device_status() == 0   # cleared
 
 
+# groups the kernels are not built for directly: padded sub-groups (3 -> 4,
+# 5/6/7 -> 8) and groups split into sub-groups of at most 8 heads (12, 16, 24)
+ANY_G_CASES = [
+    # B, H, Hkv, d, w, g, positions
+    (2, 6, 2, 128, 64, 4, [200, 5]),          # group of 3
+    (2, 5, 1, 128, 100, 2, [99, 3000]),       # group of 5
+    (3, 12, 2, 64, 50, 3, [0, 51, 777]),      # group of 6, d = 64
+    (1, 7, 1, 128, 33, 0, [40]),              # group of 7
+    (2, 24, 2, 128, 128, 4, [130, 1000]),     # group of 12: two sub-groups of 6
+    (2, 16, 1, 128, 256, 4, [300, 17]),       # group of 16: two sub-groups of 8
+    (1, 24, 1, 64, 70, 1, [500]),             # group of 24: three sub-groups of 8
+]
+
+
 @pytest.mark.gpu
-def test_decode_group_of_16_is_refused(swa):
-    x = synthetic.decode_cache_inputs(1, 16, 1, 128, 8, 0, 9, seed=0, device="cuda")
-    with pytest.raises(swa.SwaError):
-        swa.decode(x.q, x.Kc, x.Vc, x.pos, 8, 0, x.scale, num_splits=1)
+@pytest.mark.parametrize("B,H,Hkv,d,w,g,pos", ANY_G_CASES)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_any_group_matches_oracle(swa, oracle_mod, B, H, Hkv, d, w, g, pos, dtype):
+    x = synthetic.decode_cache_inputs(B, H, Hkv, d, w, g, pos, dtype=dtype, seed=H + w,
+                                      sink_scale=4.0, device="cuda")
+    O, L = oracle_mod.decode_cache(x.q, x.Kc, x.Vc, x.pos.cpu().numpy(), w, g, x.scale)
+    for splits in (0, 1, 3):
+        lse = torch.empty(B, H, dtype=torch.float32, device="cuda")
+        out = torch.full_like(x.q, float("nan"))
+        swa.decode(x.q, x.Kc, x.Vc, x.pos, w, g, x.scale, out=out, lse=lse, num_splits=splits)
+        torch.cuda.synchronize()
+        assert_close(out, O, dtype, f"decode G={H // Hkv} splits={splits}")
+        tol = 2e-3 if dtype == "bf16" else 1e-5
+        assert np.abs(lse.cpu().double().numpy() - L).max() < tol
+    if dtype == "bf16":  # the library-workspace entry point too
+        out = swa.decode(x.q, x.Kc, x.Vc, x.pos, w, g, x.scale)
+        torch.cuda.synchronize()
+        assert_close(out, O, dtype, f"swa_decode G={H // Hkv}")
+    assert swa.device_status() == 0
+
+
+@pytest.mark.gpu
+def test_streaming_group_of_three_matches_history(swa, oracle_mod):
+    B, H, Hkv, d, P, w, g = 2, 6, 2, 128, 30, 8, 2
+    K, V = synthetic.token_stream(B, Hkv, d, P, seed=17, device="cuda", g=g, sink_scale=4.0)
+    gen = torch.Generator(device="cuda").manual_seed(18)
+    qs = torch.randn(P, B, H, d, generator=gen, device="cuda").to(torch.bfloat16)
+    Kc = torch.zeros(B, Hkv, w + g, d, dtype=K.dtype, device="cuda")
+    Vc = torch.zeros_like(Kc)
+    for p in range(P):
+        pos = torch.full((B,), p, dtype=torch.int32, device="cuda")
+        swa.cache_append(Kc, Vc, K[:, :, p:p + 1].contiguous(), V[:, :, p:p + 1].contiguous(),
+                         pos, w, g)
+        out = swa.decode(qs[p], Kc, Vc, pos, w, g, 0.125)
+        torch.cuda.synchronize()
+        O, _ = oracle_mod.decode_history(qs[p], K, V, np.full(B, p), w, g, 0.125)
+        assert_close(out, O, "bf16", f"stream G=3 p={p}")
+    assert swa.device_status() == 0
