@@ -771,6 +771,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // it through STAGE_WARP bytes of shared memory per warp (store_o_rows_chunked).
 // ------------------------------------------------------------------------
 constexpr int NTHREADS2 = 512;
+// The narrow sink tile: when the sinks 0 .. g-1 (g <= NB_SINK) form a key tile
+// of their own, below the band (every item's first tile then), the pair kernel
+// loads, multiplies and exponentiates only its first NB_SINK keys: S with
+// N = NB_SINK, P V with one K-step of 16 keys.  In the window path the second
+// set of key/value maps (tmK2, tmV2) are boxes of NB_SINK rows for this tile.
+constexpr int NB_SINK = 16;
+// NS: the kernel instantiation that has the narrow sink tile (the window path
+// with 1 <= g <= NB_SINK); the others carry none of its code.
+template <bool PAT, bool NS>
+__device__ __forceinline__ bool narrow_sink_tile(const TileRange &tr, int j, const PrefillParams &p)
+{
+    if constexpr (PAT || !NS) return false;
+    return j == 0 && tr.ns == 1 && p.g <= NB_SINK;
+}
 // named barriers 1 (head A) and 2 (head B): a softmax warpgroup's 128 threads
 // arrive when P is in tensor memory, the 32 threads of the MMA warp wait
 constexpr int P_BAR_THREADS = 128 + 32;
@@ -881,7 +895,7 @@ __device__ __forceinline__ void softmax_half(const uint32_t (&sa)[32], const uin
     }
 }
 
-template <int HD, bool PAT, bool QP>
+template <int HD, bool PAT, bool QP, bool NS>
 __global__ void __launch_bounds__(NTHREADS2, 1)
     swa_prefill_bf16_pair_sm103(const __grid_constant__ CUtensorMap tmQ,
                                 const __grid_constant__ CUtensorMap tmK,
@@ -987,14 +1001,18 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     // warp's wait for them runs out (nothing is in flight to drain)
                     if (p.skip_first_kv && kv_iter == 0) continue;
                     // K and V of a stage complete one barrier: the MMA issuer waits
-                    // once per key tile
-                    mbar_expect_tx(BAR(L::K_FULL + st), 2 * L::KB);
+                    // once per key tile.  The narrow sink tile is NB_SINK rows at
+                    // the top of each 64-column chunk (the tmK2/tmV2 boxes).
+                    const bool nar = narrow_sink_tile<PAT, NS>(tr, j, p);
+                    const CUtensorMap *mk = nar ? &tmK2 : hi ? &tmK : &tmK2;
+                    const CUtensorMap *mv = nar ? &tmV2 : hi ? &tmV : &tmV2;
+                    mbar_expect_tx(BAR(L::K_FULL + st), nar ? 2u * NB_SINK * HD * 2 : 2 * L::KB);
                     for (int c = 0; c < HD / 64; ++c)
-                        load_rows<PAT>(sK + st * L::KB + c * (BN * 128), hi ? &tmK : &tmK2,
-                                    BAR(L::K_FULL + st), c * 64, kc, kt.k0, zkv);
+                        load_rows<PAT>(sK + st * L::KB + c * (BN * 128), mk, BAR(L::K_FULL + st),
+                                       c * 64, kc, kt.k0, zkv);
                     for (int c = 0; c < HD / 64; ++c)
-                        load_rows<PAT>(sV + st * L::KB + c * (BN * 128), hi ? &tmV : &tmV2,
-                                    BAR(L::K_FULL + st), c * 64, kc, kt.k0, zkv);
+                        load_rows<PAT>(sV + st * L::KB + c * (BN * 128), mv, BAR(L::K_FULL + st),
+                                       c * 64, kc, kt.k0, zkv);
                     last_k_par[st] = static_cast<int>(ph);
                 }
             }
@@ -1017,10 +1035,11 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         // group and the K-steps are unrolled with compile-time offsets.
         {
             const uint32_t idesc_s = idesc_bf16_f32(128, BN, 0);
+            const uint32_t idesc_s16 = idesc_bf16_f32(128, NB_SINK, 0);
             const uint32_t idesc_o = idesc_bf16_f32(128, HD, 1);
             int kv_iter = 0, it = 0, c = 0;
             bool ok = true;
-            bool have_prev = false, prev_first = false, prev_last = false;
+            bool have_prev = false, prev_first = false, prev_last = false, prev_narrow = false;
             int prev_st = 0, prev_c = 0, prev_it = 0;
             // P_X(prev) V into O_X
             auto issue_pv = [&](auto xc) -> bool {
@@ -1038,18 +1057,21 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 tc_fence_after();
                 const uint64_t vb = smem_desc_sw128(sV + prev_st * L::KB, BN * 128, 1024);
                 const uint32_t o_t = tmem + x * 256, p_t = tmem + x * 256 + 128;
-                mma_ts_group8(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
+                if (prev_narrow)  // the narrow sink tile: one K-step of 16 keys
+                    mma_ts_e(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
+                else
+                    mma_ts_group8(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
                 if (x == 1) tc_commit_e(BAR(L::KV_EMPTY + prev_st));
                 if (prev_last) tc_commit_e(BAR(L::O_FULL + x));
                 return true;
             };
             // S_X = Q_X K^T
-            auto issue_s = [&](auto xc, int st, bool last) {
+            auto issue_s = [&](auto xc, int st, bool last, bool narrow) {
                 constexpr int x = decltype(xc)::value;
                 const uint64_t qb = smem_desc_sw128(sQ + x * L::QB, 16, 1024);
                 const uint64_t kb = smem_desc_sw128(sK + st * L::KB, 16, 1024);
                 const uint32_t s_t = tmem + x * 256 + 128;
-                mma_ss_group<HD / 16>(s_t, qb, kb, idesc_s);
+                mma_ss_group<HD / 16>(s_t, qb, kb, narrow ? idesc_s16 : idesc_s);
                 tc_commit_e(BAR(L::S_FULL + x));
                 if (last) tc_commit_e(BAR(L::Q_EMPTY + x));
             };
@@ -1065,6 +1087,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
                     const bool last = (j == tr.count - 1);
+                    const bool narrow = narrow_sink_tile<PAT, NS>(tr, j, p);
                     // head A: P_A(c-1) V, then S_A(c)
                     if (have_prev && !issue_pv(X0{})) {
                         ok = false;
@@ -1076,7 +1099,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         break;
                     }
                     tc_fence_after();
-                    issue_s(X0{}, st, last);
+                    issue_s(X0{}, st, last, narrow);
                     // head B: P_B(c-1) V, then S_B(c)
                     if (have_prev && !issue_pv(X1{})) {
                         ok = false;
@@ -1087,13 +1110,14 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         break;
                     }
                     tc_fence_after();
-                    issue_s(X1{}, st, last);
+                    issue_s(X1{}, st, last, narrow);
                     have_prev = true;
                     prev_st = st;
                     prev_c = c;
                     prev_it = it;
                     prev_first = (j == 0);
                     prev_last = last;
+                    prev_narrow = narrow;
                 }
             }
             if (ok && have_prev) {
@@ -1156,6 +1180,38 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     break;
                 }
                 tc_fence_after();
+                if (narrow_sink_tile<PAT, NS>(tr, j, p)) {
+                    // the item's first tile: NB_SINK sink keys (key indices 0 ..),
+                    // masked with the general rule; m starts here
+                    uint32_t sn[NB_SINK];
+                    tmem_ld16(s_addr, sn);
+                    tmem_ld_wait();
+                    reg_fence16(sn);
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < NB_SINK; ++e) {
+                        if (!(e <= i && (e >= lo || e < p.g))) sn[e] = __float_as_uint(-INFINITY);
+                        mx = fmaxf(mx, __uint_as_float(sn[e]));
+                    }
+                    m = mx * sl2;
+                    const float m_use = (m == -INFINITY) ? 0.f : m;
+                    uint32_t pn[NB_SINK / 2];
+                    float ls = 0.f;
+#pragma unroll
+                    for (int e = 0; e < NB_SINK; e += 2) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sn[e]), sl2, -m_use));
+                        const float p1 = ex2(fmaf(__uint_as_float(sn[e + 1]), sl2, -m_use));
+                        ls += p0 + p1;
+                        pn[e >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    l = ls;
+                    tmem_st8(s_addr, pn);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    p_arrive(x);
+                    continue;
+                }
                 uint32_t s[4][32];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tmem_ld32(s_addr + q * 32, s[q]);
@@ -1470,44 +1526,61 @@ bool make_view(CUtensorMap *m, const void *base, uint64_t d, uint64_t R, uint64_
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One launch of the pair kernel: head pairs of an even group, or (QP) pairs of
+// adjacent q tiles of one head for an odd group.
+template <int HD, bool PAT, bool QP, bool NS>
+int launch_pair(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
+                PrefillParams p, int per_unit, cudaStream_t stream)
+{
+    using L2 = Layout2<HD>;
+    if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS>>(L2::DYN_SMEM) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    if constexpr (QP) {
+        p.n_qt = (p.n + 2 * BM - 1) / (2 * BM);  // levels of q-tile pairs
+        p.num_items = p.B * p.H * p.n_qt;
+    } else {
+        p.num_items = p.B * p.Hkv * (p.G / 2) * per_unit;
+    }
+    const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
+    swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS>
+        <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
+    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
 template <int HD, bool PAT>
 int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                    const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
                    PrefillParams p, int per_unit, cudaStream_t stream)
 {
-    using L2 = Layout2<HD>;
-    if (p.G % 2 == 0) {
-        // two heads of a GQA pair per work item
-        if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, PAT, false>>(L2::DYN_SMEM) !=
-            cudaSuccess)
-            return SWA_ERR_CUDA;
-        p.num_items = p.B * p.Hkv * (p.G / 2) * per_unit;
-        const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-        swa_prefill_bf16_pair_sm103<HD, PAT, false>
-            <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
-        return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
-    }
     if constexpr (!PAT) {
-        // an odd group: two adjacent q tiles of one head per work item (the
-        // fixed patterns keep the single-head kernel below)
-        if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, false, true>>(L2::DYN_SMEM) !=
-            cudaSuccess)
+        // the window path: the narrow sink tile is compiled in only where it is
+        // used (1 <= g <= NB_SINK); an odd group pairs adjacent q tiles of one head
+        const bool ns = p.g >= 1 && p.g <= NB_SINK;
+        if (p.G % 2 == 0)
+            return ns ? launch_pair<HD, false, false, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
+                                                            stream)
+                      : launch_pair<HD, false, false, false>(mq, mk, mv, mq2, mk2, mv2, p,
+                                                             per_unit, stream);
+        return ns ? launch_pair<HD, false, true, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
+                                                       stream)
+                  : launch_pair<HD, false, true, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
+                                                        stream);
+    } else {
+        // the fixed patterns: head pairs for even groups, the single-head kernel
+        // for odd ones
+        if (p.G % 2 == 0)
+            return launch_pair<HD, true, false, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
+                                                       stream);
+        using L = Layout<HD>;
+        if (smem_opt_in<swa_prefill_bf16_sm103<HD, PAT>>(L::DYN_SMEM) != cudaSuccess)
             return SWA_ERR_CUDA;
-        p.n_qt = (p.n + 2 * BM - 1) / (2 * BM);  // levels of q-tile pairs
-        p.num_items = p.B * p.H * p.n_qt;
+        p.num_items = p.B * p.H * per_unit;
         const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-        swa_prefill_bf16_pair_sm103<HD, false, true>
-            <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
+        swa_prefill_bf16_sm103<HD, PAT>
+            <<<grid, NTHREADS, L::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
         return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
     }
-    using L = Layout<HD>;
-    if (smem_opt_in<swa_prefill_bf16_sm103<HD, PAT>>(L::DYN_SMEM) != cudaSuccess)
-        return SWA_ERR_CUDA;
-    p.num_items = p.B * p.H * per_unit;
-    const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-    swa_prefill_bf16_sm103<HD, PAT>
-        <<<grid, NTHREADS, L::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
-    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
 template <int HD>
@@ -1524,11 +1597,11 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     CUtensorMap mq, mk, mv, mq2, mk2, mv2;
     bool ok;
     if (!pat) {
+        // the second key/value maps are the narrow sink tile's boxes of NB_SINK rows
         ok = make_map_3d(&mq, Q, HD, n, ZQ, BM) && make_map_3d(&mk, K, HD, n_k, ZK, BN) &&
-             make_map_3d(&mv, V, HD, n_k, ZK, BN);
+             make_map_3d(&mv, V, HD, n_k, ZK, BN) && make_map_3d(&mk2, K, HD, n_k, ZK, NB_SINK) &&
+             make_map_3d(&mv2, V, HD, n_k, ZK, NB_SINK);
         mq2 = mq;
-        mk2 = mk;
-        mv2 = mv;
     } else if (rl > 0) {
         // landmarks: Q, K, V as they are, and K, V as the stride-rl view whose
         // class 0 lists positions 0, rl, 2 rl, ... (ceil(n/rl) of them)

@@ -40,6 +40,38 @@ def test_prefill_bf16_matches_oracle(swa, oracle_mod, B, H, Hkv, n, d, w, g):
     assert np.abs(lse.cpu().double().numpy() - L).max() < 2e-3
 
 
+# The narrow sink tile: once the band of a 128-row query tile starts past key
+# tile 0, the sinks 0..g-1 (g <= 16) are read through a 16-key tile.  Shapes
+# with n well past w + 128, so most query tiles take it; g = 16 is the widest
+# narrow tile, g = 17 the narrowest full one; odd groups (q-tile pairs) too.
+NARROW_SINK_CASES = [
+    # B, H, Hkv, n, d, w, g
+    (1, 4, 2, 900, 128, 100, 1),
+    (2, 2, 1, 1000, 128, 64, 4),
+    (1, 2, 1, 700, 64, 128, 16),
+    (1, 2, 1, 700, 128, 128, 17),
+    (1, 3, 1, 800, 128, 200, 4),     # a group of 3: q-tile pairs of one head
+    (1, 1, 1, 1100, 64, 1, 5),       # window of one: only the sink tile and the diagonal
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,H,Hkv,n,d,w,g", NARROW_SINK_CASES)
+def test_prefill_narrow_sink_tile_matches_oracle(swa, oracle_mod, B, H, Hkv, n, d, w, g):
+    x = synthetic.prefill_inputs(B, H, Hkv, n, d, w, g, dtype="bf16", seed=n + g, sink_scale=4.0,
+                                 device="cuda")
+    lse = torch.empty(B, H, n, dtype=torch.float32, device="cuda")
+    sink = torch.linspace(-2.0, 3.0, H, device="cuda", dtype=torch.float32)
+    for sl in (None, sink):
+        out = swa.prefill(x.Q, x.K, x.V, w, g, x.scale, lse=lse, sink_logit=sl)
+        torch.cuda.synchronize()
+        O, L = oracle_mod.prefill(x.Q, x.K, x.V, w, g, x.scale,
+                                  sink_logit=None if sl is None else sl.cpu())
+        assert_close(out, O, "bf16", f"O {B,H,Hkv,n,d,w,g} sink_logit={sl is not None}")
+        assert np.abs(lse.cpu().double().numpy() - L).max() < 2e-3
+    assert swa.device_status() == 0
+
+
 @pytest.mark.gpu
 def test_prefill_bf16_window_one_is_value(swa):
     x = synthetic.prefill_inputs(1, 2, 1, 700, 128, 1, 0, dtype="bf16", seed=3, device="cuda")
