@@ -805,9 +805,9 @@ struct Layout2 {
     enum {
         Q_FULL = 0,
         Q_EMPTY = 2,
-        K_FULL = 4,
-        V_FULL = K_FULL + STAGES,
-        KV_EMPTY = V_FULL + STAGES,
+        K_FULL = 4,                  // K(c) and V(c-1) have landed (tile c's barrier)
+        V_EMPTY = K_FULL + STAGES,   // a V slot is free (after the second head's P V)
+        KV_EMPTY = V_EMPTY + STAGES, // a K slot is free (after the second head's S)
         S_FULL = KV_EMPTY + STAGES,
         P_FULL = S_FULL + 2,
         O_FULL = P_FULL + 2,
@@ -930,7 +930,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         }
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(BAR(L::K_FULL + i), 1);
-            mbar_init(BAR(L::V_FULL + i), 1);
+            mbar_init(BAR(L::V_EMPTY + i), 1);
             mbar_init(BAR(L::KV_EMPTY + i), 1);
         }
         mbar_init(BAR(L::DRAIN), 1);
@@ -963,6 +963,29 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             int last_k_par[STAGES], last_q_par[2] = {-1, -1};
             for (int s = 0; s < STAGES; ++s) last_k_par[s] = -1;
             bool ok = true;
+            // Tile c's barrier (K_FULL slot c % STAGES) carries K(c) and V(c-1): the
+            // K slot is freed after the second head's S (a tile earlier than a
+            // combined K/V stage would be), so K(c) is requested a whole tile
+            // period before S_A(c) needs it, and the MMA warp still waits once per
+            // tile.  The last tile's V rides on the barrier of the tile after it.
+            // pv_*: the previous tile's V, still to be loaded.
+            bool pv_have = false, pv_nar = false;
+            int pv_k0 = 0, pv_kc = 0, pv_z = 0;
+            const CUtensorMap *pv_map = &tmV;
+            // waits until V slot (c_next - 1) % STAGES is free for V(c_next - 1)
+            auto load_prev_v = [&](int c_next) -> bool {
+                const int vc = c_next - 1, vs = vc % STAGES;
+                if (!mbar_wait(BAR(L::V_EMPTY + vs), ((vc / STAGES) & 1) ^ 1, abort_flag, p.status,
+                               p.wait_ns))
+                    return false;
+                return true;
+            };
+            auto issue_prev_v = [&](int c_next, uint32_t bar) {
+                const int vs = (c_next - 1) % STAGES;
+                for (int c = 0; c < HD / 64; ++c)
+                    load_rows<PAT>(sV + vs * L::KB + c * (BN * 128), pv_map, bar, c * 64, pv_kc,
+                                   pv_k0, pv_z);
+            };
             for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
                  t = pair_item_rank(blockIdx.x, ++it)) {
                 int b, hp, kvh, qt, cls;
@@ -987,7 +1010,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
-                    if (!mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status,
+                    if ((pv_have && !load_prev_v(kv_iter)) ||
+                        !mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status,
                                    p.wait_ns)) {
                         ok = false;
                         break;
@@ -999,20 +1023,44 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     const bool hi = !PAT || kt.land || cls < p.rem;
                     // test injection: this stage's copies never start, so the MMA
                     // warp's wait for them runs out (nothing is in flight to drain)
-                    if (p.skip_first_kv && kv_iter == 0) continue;
-                    // K and V of a stage complete one barrier: the MMA issuer waits
-                    // once per key tile.  The narrow sink tile is NB_SINK rows at
-                    // the top of each 64-column chunk (the tmK2/tmV2 boxes).
+                    if (p.skip_first_kv && kv_iter == 0) {
+                        pv_have = false;
+                        continue;
+                    }
+                    // this tile's K and the previous tile's V complete this tile's
+                    // barrier.  The narrow sink tile is NB_SINK rows at the top of
+                    // each 64-column chunk (the tmK2/tmV2 boxes).
                     const bool nar = narrow_sink_tile<PAT, NS>(tr, j, p);
                     const CUtensorMap *mk = nar ? &tmK2 : hi ? &tmK : &tmK2;
                     const CUtensorMap *mv = nar ? &tmV2 : hi ? &tmV : &tmV2;
-                    mbar_expect_tx(BAR(L::K_FULL + st), nar ? 2u * NB_SINK * HD * 2 : 2 * L::KB);
+                    const uint32_t kbytes = nar ? 1u * NB_SINK * HD * 2 : L::KB;
+                    const uint32_t vbytes = !pv_have ? 0u : pv_nar ? 1u * NB_SINK * HD * 2 : L::KB;
+                    mbar_expect_tx(BAR(L::K_FULL + st), kbytes + vbytes);
+                    if (pv_have) issue_prev_v(kv_iter, BAR(L::K_FULL + st));
                     for (int c = 0; c < HD / 64; ++c)
                         load_rows<PAT>(sK + st * L::KB + c * (BN * 128), mk, BAR(L::K_FULL + st),
                                        c * 64, kc, kt.k0, zkv);
-                    for (int c = 0; c < HD / 64; ++c)
-                        load_rows<PAT>(sV + st * L::KB + c * (BN * 128), mv, BAR(L::K_FULL + st),
-                                       c * 64, kc, kt.k0, zkv);
+                    last_k_par[st] = static_cast<int>(ph);
+                    pv_have = true;
+                    pv_nar = nar;
+                    pv_k0 = kt.k0;
+                    pv_kc = kc;
+                    pv_z = zkv;
+                    pv_map = mv;
+                }
+            }
+            // the last tile's V, on the barrier of the tile after it
+            if (ok && pv_have) {
+                const int st = kv_iter % STAGES;
+                const uint32_t ph = (kv_iter / STAGES) & 1;
+                // the barrier's previous phase (tile kv_iter - 2) must be complete
+                // before it is armed again: its K slot release says so
+                if (!load_prev_v(kv_iter) ||
+                    !mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status, p.wait_ns)) {
+                    ok = false;
+                } else {
+                    mbar_expect_tx(BAR(L::K_FULL + st), pv_nar ? 1u * NB_SINK * HD * 2 : L::KB);
+                    issue_prev_v(kv_iter, BAR(L::K_FULL + st));
                     last_k_par[st] = static_cast<int>(ph);
                 }
             }
@@ -1050,7 +1098,6 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 // the abort flag, which is checked after every meeting, so this
                 // never waits for an arrival that will not come.
                 asm volatile("bar.sync %0, %1;" ::"n"(1 + x), "n"(P_BAR_THREADS) : "memory");
-                if (*abort_flag) return false;
                 if (prev_first && !warp_wait(BAR(L::O_EMPTY + x), (prev_it & 1) ^ 1, abort_flag,
                                              p.status, p.wait_ns))
                     return false;
@@ -1061,9 +1108,11 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     mma_ts_e(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
                 else
                     mma_ts_group8(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
-                if (x == 1) tc_commit_e(BAR(L::KV_EMPTY + prev_st));
+                if (x == 1) tc_commit_e(BAR(L::V_EMPTY + prev_st));
                 if (prev_last) tc_commit_e(BAR(L::O_FULL + x));
-                return true;
+                // a softmax warpgroup that gave up arrived once more on the barrier
+                // above; the product just issued read a garbage P, which is harmless
+                return !*abort_flag;
             };
             // S_X = Q_X K^T
             auto issue_s = [&](auto xc, int st, bool last, bool narrow) {
@@ -1074,6 +1123,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 mma_ss_group<HD / 16>(s_t, qb, kb, narrow ? idesc_s16 : idesc_s);
                 tc_commit_e(BAR(L::S_FULL + x));
                 if (last) tc_commit_e(BAR(L::Q_EMPTY + x));
+                if (x == 1) tc_commit_e(BAR(L::KV_EMPTY + st));
             };
             using X0 = std::integral_constant<int, 0>;
             using X1 = std::integral_constant<int, 1>;
@@ -1088,13 +1138,17 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     const uint32_t ph = (kv_iter / STAGES) & 1;
                     const bool last = (j == tr.count - 1);
                     const bool narrow = narrow_sink_tile<PAT, NS>(tr, j, p);
+                    // K(c) and V(c-1) have landed: one wait per tile
+                    if (!warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
                     // head A: P_A(c-1) V, then S_A(c)
                     if (have_prev && !issue_pv(X0{})) {
                         ok = false;
                         break;
                     }
-                    if ((j == 0 && !warp_wait(BAR(L::Q_FULL + 0), it & 1, abort_flag, p.status, p.wait_ns)) ||
-                        !warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, p.wait_ns)) {
+                    if (j == 0 && !warp_wait(BAR(L::Q_FULL + 0), it & 1, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -1120,7 +1174,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     prev_narrow = narrow;
                 }
             }
-            if (ok && have_prev) {
+            if (ok && have_prev &&
+                warp_wait(BAR(L::K_FULL + kv_iter % STAGES), (kv_iter / STAGES) & 1, abort_flag,
+                          p.status, p.wait_ns)) {
                 if (issue_pv(X0{})) issue_pv(X1{});
             }
             // drain: every MMA this warp issued has completed before exit
