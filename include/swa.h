@@ -347,6 +347,29 @@ int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_sl
 int swa_get_device_status(swa_stream_t stream);
 
 /*
+ * swa_debug_prefill_walk -- a diagnostic with no counterpart on the pages: runs
+ * swa_prefill_pattern (bf16, tensor-core kernels; no lse, no sink logit) and
+ * logs every key tile the kernels' producers load, so that a test can compare
+ * the tile walk the kernels actually take with the tile set the method
+ * defines ("Sliding Window and Sparse Attention, from Longformer to CSA2",
+ * section 4: only the key tiles that meet the band or the sinks are read).
+ * log: device int32, 16-byte aligned, 8 + 8 * log_entries elements; log[0]
+ * counts the tiles loaded (entries past log_entries are counted, not stored);
+ * entry e at log[8 + 8e] is {work item rank, sequence b, kv head, unit, q tile,
+ * residue class, first key index of the tile, flags}.  The unit is the head
+ * pair (even groups: heads kvh*G + 2u, +1), the q-tile pair of head kvh*G + u
+ * (odd groups, window and sinks: q tiles 2*qtile and 2*qtile + 1), or the head
+ * kvh*G + u (odd groups under the other patterns); q tiles and key indices
+ * count 128-row tiles and rows of the residue class's subsequence for the
+ * dilated and strided patterns, and landmark-list entries for landmark tiles.
+ * flags: 1 the tile needs no element mask, 2 a landmark tile, 4 the narrow sink
+ * tile (16 keys).  Returns as swa_prefill_pattern.
+ */
+int swa_debug_prefill_walk(const void *Q, const void *K, const void *V, void *O, int B, int H,
+                           int Hkv, int n, int d, swa_pattern pattern, int w, int g, int r,
+                           float scale, int32_t *log, int64_t log_entries, swa_stream_t stream);
+
+/*
  * swa_debug_inject_stall -- a test aid with no counterpart on the pages; it
  * lets a test run the kernels' timeout path without faulting or hanging the
  * GPU.  The next launch of the chosen kind on the current device leaves out

@@ -29,7 +29,7 @@ __all__ = [
     "SwaError", "prefill", "prefill_pattern", "prefill_chunk", "prefill_chunk_workspace_bytes",
     "PATTERNS", "decode", "cache_append", "decode_workspace_bytes",
     "count_pairs", "enumerate_tiles", "enumerate_landmark_tiles", "chunk_key_positions",
-    "cache_slot", "device_status", "inject_stall",
+    "cache_slot", "device_status", "inject_stall", "prefill_walk",
     "selftest_umma",
     "library_path", "lib",
 ]
@@ -67,6 +67,7 @@ SIGNATURES = {
     "swa_cache_slot": (_i, [_i64, _i, _i, _p, _p]),
     "swa_get_device_status": (_i, [_p]),
     "swa_debug_inject_stall": (_i, [_i, _i64]),
+    "swa_debug_prefill_walk": (_i, [_p] * 4 + [_i] * 5 + [_i] * 4 + [_f, _p, _i64, _p]),
     "swa_status_string": (ctypes.c_char_p, [_i]),
     "swa_version": (_i, []),
     "swa_selftest_umma": (_i, [_p, _p, _p, _p, _p, _p]),
@@ -349,6 +350,34 @@ def cache_slot(p: int, w: int, g: int):
 def device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status code."""
     return int(_load().swa_get_device_status(_stream(stream, None)))
+
+
+WALK_FIELDS = ("item", "b", "kvh", "unit", "qtile", "cls", "k0", "flags")
+
+
+def prefill_walk(q, k, v, pattern: str, w: int, g: int = 0, r: int = 1,
+                 scale: float | None = None, max_entries: int = 1 << 20, stream=None):
+    """Diagnostic (swa_debug_prefill_walk): runs the bf16 prefill and returns
+    (out, entries) where entries is an int32 CPU tensor [m, 8] of the key tiles
+    the kernels loaded, columns WALK_FIELDS, and m the number loaded."""
+    _need(q, "q", torch.bfloat16)
+    B, H, n, d = q.shape
+    Hkv = k.shape[1]
+    _need(k, "k", torch.bfloat16, (B, Hkv, n, d))
+    _need(v, "v", torch.bfloat16, (B, Hkv, n, d))
+    out = torch.empty_like(q)
+    log = torch.zeros(8 + 8 * max_entries, dtype=torch.int32, device=q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = _stream(stream, q.device)
+    rc = _load().swa_debug_prefill_walk(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Hkv, n, d,
+                                        PATTERNS[pattern], int(w), int(g), int(r), scale,
+                                        _ptr(log), max_entries, st)
+    _check("swa_debug_prefill_walk", rc)
+    torch.cuda.synchronize(q.device)
+    m = int(log[0].item())
+    if m > max_entries:
+        raise RuntimeError(f"the walk has {m} tiles, more than max_entries={max_entries}")
+    return out, log[8:8 + 8 * m].view(m, 8).cpu()
 
 
 STALL_KINDS = {"prefill": 1, "decode": 2}

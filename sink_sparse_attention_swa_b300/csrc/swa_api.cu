@@ -112,23 +112,28 @@ int swa_prefill_sink_logit(const void *Q, const void *K, const void *V, void *O,
     return SWA_ERR_INVALID_ARG;
 }
 
-int swa_prefill_pattern(const void *Q, const void *K, const void *V, void *O, float *lse,
-                        const float *sink_logit, int B, int H, int Hkv, int n, int d,
-                        swa_pattern pattern, int w, int g, int r, float scale, swa_dtype dtype,
-                        swa_stream_t stream)
+}  // extern "C"
+
+namespace {
+// swa_prefill_pattern, with an optional tile-walk log for the bf16 kernels.
+int prefill_pattern_impl(const void *Q, const void *K, const void *V, void *O, float *lse,
+                         const float *sink_logit, int B, int H, int Hkv, int n, int d,
+                         swa_pattern pattern, int w, int g, int r, float scale, swa_dtype dtype,
+                         swa_stream_t stream, int32_t *walk, long long walk_cap)
 {
-    if (pattern == SWA_PATTERN_WINDOW)
+    if (pattern == SWA_PATTERN_WINDOW && walk == nullptr)
         return swa_prefill_sink_logit(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, d, w, g, scale,
                                       dtype, stream);
-    if (pattern != SWA_PATTERN_DILATED && pattern != SWA_PATTERN_STRIDED &&
-        pattern != SWA_PATTERN_LANDMARK)
+    if (pattern != SWA_PATTERN_WINDOW && pattern != SWA_PATTERN_DILATED &&
+        pattern != SWA_PATTERN_STRIDED && pattern != SWA_PATTERN_LANDMARK)
         return SWA_ERR_INVALID_ARG;
     if (r < 1 || n < 1 || n > INT32_MAX - 256) return SWA_ERR_INVALID_ARG;
     if (pattern == SWA_PATTERN_STRIDED) w = n;  // no limit on the number of strides back
     int rc = check_heads(B, H, Hkv, d, w, g);
     if (rc != SWA_OK) return rc;
     // residue classes carry no sink columns (a sink below g belongs to one class only)
-    if (pattern != SWA_PATTERN_LANDMARK && g != 0) return SWA_ERR_UNSUPPORTED;
+    if ((pattern == SWA_PATTERN_DILATED || pattern == SWA_PATTERN_STRIDED) && g != 0)
+        return SWA_ERR_UNSUPPORTED;
     if (!scale_ok(scale)) return SWA_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SWA_ERR_INVALID_ARG;
     if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
@@ -137,7 +142,7 @@ int swa_prefill_pattern(const void *Q, const void *K, const void *V, void *O, fl
     int R = 1, rl = 0, wk = w;
     if (pattern == SWA_PATTERN_LANDMARK) {
         rl = r;
-    } else {
+    } else if (pattern != SWA_PATTERN_WINDOW) {
         R = r < n ? r : n;  // strides past the sequence: each class is one row
         const int rows = (n + R - 1) / R;
         if (pattern == SWA_PATTERN_STRIDED || wk > rows) wk = rows;
@@ -150,11 +155,37 @@ int swa_prefill_pattern(const void *Q, const void *K, const void *V, void *O, fl
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == SWA_BF16)
         return launch_prefill_bf16(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, wk, g, scale,
-                                   nullptr, R, rl, st);
+                                   nullptr, R, rl, st, walk, walk_cap);
+    if (walk != nullptr) return SWA_ERR_UNSUPPORTED;  // the log is of the tensor-core kernels
     if (dtype == SWA_F32)
         return launch_prefill_f32(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, wk, g, scale,
                                   nullptr, R, rl, st);
     return SWA_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+int swa_prefill_pattern(const void *Q, const void *K, const void *V, void *O, float *lse,
+                        const float *sink_logit, int B, int H, int Hkv, int n, int d,
+                        swa_pattern pattern, int w, int g, int r, float scale, swa_dtype dtype,
+                        swa_stream_t stream)
+{
+    return prefill_pattern_impl(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, d, pattern, w, g, r,
+                                scale, dtype, stream, nullptr, 0);
+}
+
+int swa_debug_prefill_walk(const void *Q, const void *K, const void *V, void *O, int B, int H,
+                           int Hkv, int n, int d, swa_pattern pattern, int w, int g, int r,
+                           float scale, int32_t *log, int64_t log_entries, swa_stream_t stream)
+{
+    if (log == nullptr || (reinterpret_cast<uintptr_t>(log) & 15u) || log_entries < 0)
+        return SWA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(log, 0, 8 * sizeof(int32_t), st) != cudaSuccess) return SWA_ERR_CUDA;
+    return prefill_pattern_impl(Q, K, V, O, nullptr, nullptr, B, H, Hkv, n, d, pattern, w, g, r,
+                                scale, SWA_BF16, stream, log, log_entries);
 }
 
 size_t swa_prefill_chunk_workspace_bytes(int B, int Hkv, int T, int d, int w, int g,

@@ -113,7 +113,31 @@ struct PrefillParams {
     int *status;
     uint64_t wait_ns;   // limit of every bounded wait of the roles (2 s unless a test sets it)
     int skip_first_kv;  // test injection: the first key/value copy is left out (see swa.h)
+    int32_t *walk;      // tile-walk log (swa_debug_prefill_walk) or null
+    long long walk_cap; // entries the log holds
 };
+
+// One entry of the tile-walk log per key tile a producer issues: the item's
+// rank, sequence, kv head, unit (head pair, head, or q-tile pair), q tile,
+// residue class, the tile's first key index, and flags (1 full, 2 landmark
+// tile, 4 narrow sink tile).  walk[0] counts the entries; entry e is at
+// walk[WALK_HDR + WALK_ENTRY * e].
+constexpr int WALK_HDR = 8, WALK_ENTRY = 8;
+__device__ __forceinline__ void log_walk(const PrefillParams &p, int t, int b, int kvh, int u, int qt,
+                                         int cls, int k0, int flags)
+{
+    const long long e = atomicAdd(p.walk, 1);
+    if (e >= p.walk_cap) return;
+    int32_t *w = p.walk + WALK_HDR + WALK_ENTRY * e;
+    w[0] = t;
+    w[1] = b;
+    w[2] = kvh;
+    w[3] = u;
+    w[4] = qt;
+    w[5] = cls;
+    w[6] = k0;
+    w[7] = flags;
+}
 
 // Work order of both kernels.  Items are ranked by q tile, the last q tile
 // (the most key tiles) first; within a q tile by unit (query head, or head
@@ -452,6 +476,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // landmark tiles: class 0 of the stride-rl view; others: this class
                     const int kc = kt.land ? 0 : cls;
                     const bool hi = !PAT || kt.land || cls < p.rem;
+                    if (p.walk != nullptr)
+                        log_walk(p, t, b, kvh, hg, qt, cls, kt.k0,
+                                 (kt.full ? 1 : 0) | (kt.land ? 2 : 0));
                     // test injection: this stage's copies never start, so the MMA
                     // warp's wait for them runs out (nothing is in flight to drain)
                     if (p.skip_first_kv && kv_iter == 0) continue;
@@ -1031,6 +1058,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     // barrier.  The narrow sink tile is NB_SINK rows at the top of
                     // each 64-column chunk (the tmK2/tmV2 boxes).
                     const bool nar = narrow_sink_tile<PAT, NS>(tr, j, p);
+                    if (p.walk != nullptr)
+                        log_walk(p, t, b, kvh, hp, qt, cls, kt.k0,
+                                 (kt.full ? 1 : 0) | (kt.land ? 2 : 0) | (nar ? 4 : 0));
                     const CUtensorMap *mk = nar ? &tmK2 : hi ? &tmK : &tmK2;
                     const CUtensorMap *mv = nar ? &tmV2 : hi ? &tmV : &tmV2;
                     const uint32_t kbytes = nar ? 1u * NB_SINK * HD * 2 : L::KB;
@@ -1642,7 +1672,8 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
 template <int HD>
 int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, const float *sink,
               int B, int H, int Hkv, int n, int n_k, int w, int g, float scale,
-              const int32_t *pos0, int R, int rl, cudaStream_t stream)
+              const int32_t *pos0, int R, int rl, cudaStream_t stream, int32_t *walk,
+              long long walk_cap)
 {
     if (rl > 0) R = 1;
     const bool pat = R > 1 || rl > 0;
@@ -1709,6 +1740,8 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     if (p.status == nullptr) return SWA_ERR_CUDA;
     p.wait_ns = TIMEOUT_NS;
     p.skip_first_kv = take_injected_stall(SWA_STALL_PREFILL, &p.wait_ns) ? 1 : 0;
+    p.walk = walk;
+    p.walk_cap = walk_cap;
     if (pat) return launch_kernels<HD, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream);
     return launch_kernels<HD, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream);
 }
@@ -1718,14 +1751,14 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
                         const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
                         int g, float scale, const int32_t *pos0, int R, int rl,
-                        cudaStream_t stream)
+                        cudaStream_t stream, int32_t *walk, long long walk_cap)
 {
     if (d == 128)
         return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
-                              stream);
+                              stream, walk, walk_cap);
     if (d == 64)
         return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
-                             stream);
+                             stream, walk, walk_cap);
     return SWA_ERR_UNSUPPORTED;
 }
 
