@@ -1020,20 +1020,25 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 int off;
                 const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
                 const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
-                for (int x = 0; x < 2 && ok; ++x) {
-                    if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
-                                   p.wait_ns)) {
-                        ok = false;
-                        break;
+                // the item's Q tiles: issued after its first key tile (and the
+                // previous item's last value tile, which the MMA warp needs
+                // first), since their buffers free up only at the previous
+                // item's last S
+                auto load_q_tiles = [&]() -> bool {
+                    for (int x = 0; x < 2; ++x) {
+                        if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
+                                       p.wait_ns))
+                            return false;
+                        mbar_expect_tx(BAR(L::Q_FULL + x), L::QB);
+                        const int hx = pair_head<QP>(p, kvh, hp, x);
+                        const int qrow = QP ? (2 * qt + x) * BM : qt * BM;
+                        for (int c = 0; c < HD / 64; ++c)
+                            load_rows<PAT>(sQ + x * L::QB + c * (BM * 128), mq,
+                                           BAR(L::Q_FULL + x), c * 64, cls, qrow, b * p.H + hx);
+                        last_q_par[x] = it & 1;
                     }
-                    mbar_expect_tx(BAR(L::Q_FULL + x), L::QB);
-                    const int hx = pair_head<QP>(p, kvh, hp, x);
-                    const int qrow = QP ? (2 * qt + x) * BM : qt * BM;
-                    for (int c = 0; c < HD / 64; ++c)
-                        load_rows<PAT>(sQ + x * L::QB + c * (BM * 128), mq, BAR(L::Q_FULL + x),
-                                       c * 64, cls, qrow, b * p.H + hx);
-                    last_q_par[x] = it & 1;
-                }
+                    return true;
+                };
                 for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
@@ -1077,6 +1082,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     pv_kc = kc;
                     pv_z = zkv;
                     pv_map = mv;
+                    if (j == 0 && !load_q_tiles()) {
+                        ok = false;
+                        break;
+                    }
                 }
             }
             // the last tile's V, on the barrier of the tile after it
