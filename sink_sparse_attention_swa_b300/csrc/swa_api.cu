@@ -119,7 +119,7 @@ namespace {
 int prefill_pattern_impl(const void *Q, const void *K, const void *V, void *O, float *lse,
                          const float *sink_logit, int B, int H, int Hkv, int n, int d,
                          swa_pattern pattern, int w, int g, int r, float scale, swa_dtype dtype,
-                         swa_stream_t stream, int32_t *walk, long long walk_cap)
+                         swa_stream_t stream, int32_t *walk)
 {
     if (pattern == SWA_PATTERN_WINDOW && walk == nullptr)
         return swa_prefill_sink_logit(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, d, w, g, scale,
@@ -155,7 +155,7 @@ int prefill_pattern_impl(const void *Q, const void *K, const void *V, void *O, f
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == SWA_BF16)
         return launch_prefill_bf16(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, wk, g, scale,
-                                   nullptr, R, rl, st, walk, walk_cap);
+                                   nullptr, R, rl, st, walk);
     if (walk != nullptr) return SWA_ERR_UNSUPPORTED;  // the log is of the tensor-core kernels
     if (dtype == SWA_F32)
         return launch_prefill_f32(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, n, d, wk, g, scale,
@@ -173,7 +173,7 @@ int swa_prefill_pattern(const void *Q, const void *K, const void *V, void *O, fl
                         swa_stream_t stream)
 {
     return prefill_pattern_impl(Q, K, V, O, lse, sink_logit, B, H, Hkv, n, d, pattern, w, g, r,
-                                scale, dtype, stream, nullptr, 0);
+                                scale, dtype, stream, nullptr);
 }
 
 int swa_debug_prefill_walk(const void *Q, const void *K, const void *V, void *O, int B, int H,
@@ -183,9 +183,13 @@ int swa_debug_prefill_walk(const void *Q, const void *K, const void *V, void *O,
     if (log == nullptr || (reinterpret_cast<uintptr_t>(log) & 15u) || log_entries < 0)
         return SWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(log, 0, 8 * sizeof(int32_t), st) != cudaSuccess) return SWA_ERR_CUDA;
+    // header: the entry count (zero), then the capacity as a 64-bit count
+    const int64_t header[4] = {0, log_entries, 0, 0};
+    if (cudaMemcpyAsync(log, header, sizeof(header), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return SWA_ERR_CUDA;
     return prefill_pattern_impl(Q, K, V, O, nullptr, nullptr, B, H, Hkv, n, d, pattern, w, g, r,
-                                scale, SWA_BF16, stream, log, log_entries);
+                                scale, SWA_BF16, stream, log);
 }
 
 size_t swa_prefill_chunk_workspace_bytes(int B, int Hkv, int T, int d, int w, int g,

@@ -236,12 +236,13 @@ cudaError_t smem_opt_in(int bytes)
 //           pos0 == null, g == 0.
 //   rl > 0  landmarks every rl positions (add_landmarks); needs R == 1 and
 //           pos0 == null.
-// walk, walk_cap: a diagonal log of the key tiles the kernel visits (see
-// swa_debug_prefill_walk), or null for a plain launch.
+// walk: a diagnostic log of the key tiles the kernels load (the layout of
+// swa_debug_prefill_walk, its capacity in its header), or null for a plain
+// launch.
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
                         const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
                         int g, float scale, const int32_t *pos0, int R, int rl,
-                        cudaStream_t stream, int32_t *walk = nullptr, long long walk_cap = 0);
+                        cudaStream_t stream, int32_t *walk = nullptr);
 int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
                        const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
                        int g, float scale, const int32_t *pos0, int R, int rl,

@@ -113,22 +113,23 @@ struct PrefillParams {
     int *status;
     uint64_t wait_ns;   // limit of every bounded wait of the roles (2 s unless a test sets it)
     int skip_first_kv;  // test injection: the first key/value copy is left out (see swa.h)
-    int32_t *walk;      // tile-walk log (swa_debug_prefill_walk) or null
-    long long walk_cap; // entries the log holds
 };
 
 // One entry of the tile-walk log per key tile a producer issues: the item's
 // rank, sequence, kv head, unit (head pair, head, or q-tile pair), q tile,
 // residue class, the tile's first key index, and flags (1 full, 2 landmark
-// tile, 4 narrow sink tile).  walk[0] counts the entries; entry e is at
-// walk[WALK_HDR + WALK_ENTRY * e].
+// tile, 4 narrow sink tile).  log[0] counts the entries, log[2..3] holds the
+// capacity (a 64-bit count of entries); entry e is at log[WALK_HDR +
+// WALK_ENTRY * e].  The log is a kernel argument of its own, null for every
+// launch but swa_debug_prefill_walk's, kept out of PrefillParams (a larger
+// parameter block made the control warpgroup spill).
 constexpr int WALK_HDR = 8, WALK_ENTRY = 8;
-__device__ __forceinline__ void log_walk(const PrefillParams &p, int t, int b, int kvh, int u, int qt,
-                                         int cls, int k0, int flags)
+__device__ __forceinline__ void log_walk(int32_t *log, int t, int b, int kvh, int u, int qt, int cls,
+                                         int k0, int flags)
 {
-    const long long e = atomicAdd(p.walk, 1);
-    if (e >= p.walk_cap) return;
-    int32_t *w = p.walk + WALK_HDR + WALK_ENTRY * e;
+    const long long e = atomicAdd(log, 1);
+    if (e >= *reinterpret_cast<const long long *>(log + 2)) return;
+    int32_t *w = log + WALK_HDR + WALK_ENTRY * e;
     w[0] = t;
     w[1] = b;
     w[2] = kvh;
@@ -383,7 +384,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                            const __grid_constant__ CUtensorMap tmV,
                            const __grid_constant__ CUtensorMap tmQ2,
                            const __grid_constant__ CUtensorMap tmK2,
-                           const __grid_constant__ CUtensorMap tmV2, const PrefillParams p)
+                           const __grid_constant__ CUtensorMap tmV2, const PrefillParams p,
+                           int32_t *walk)
 {
     using L = Layout<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -476,8 +478,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // landmark tiles: class 0 of the stride-rl view; others: this class
                     const int kc = kt.land ? 0 : cls;
                     const bool hi = !PAT || kt.land || cls < p.rem;
-                    if (p.walk != nullptr)
-                        log_walk(p, t, b, kvh, hg, qt, cls, kt.k0,
+                    if (walk != nullptr)
+                        log_walk(walk, t, b, kvh, hg, qt, cls, kt.k0,
                                  (kt.full ? 1 : 0) | (kt.land ? 2 : 0));
                     // test injection: this stage's copies never start, so the MMA
                     // warp's wait for them runs out (nothing is in flight to drain)
@@ -922,16 +924,23 @@ __device__ __forceinline__ void softmax_half(const uint32_t (&sa)[32], const uin
     }
 }
 
-template <int HD, bool PAT, bool QP, bool NS>
+template <int HD, bool PAT, bool QP, bool NS, bool SKEW>
 __global__ void __launch_bounds__(NTHREADS2, 1)
     swa_prefill_bf16_pair_sm103(const __grid_constant__ CUtensorMap tmQ,
                                 const __grid_constant__ CUtensorMap tmK,
                                 const __grid_constant__ CUtensorMap tmV,
                                 const __grid_constant__ CUtensorMap tmQ2,
                                 const __grid_constant__ CUtensorMap tmK2,
-                                const __grid_constant__ CUtensorMap tmV2, const PrefillParams p)
+                                const __grid_constant__ CUtensorMap tmV2, const PrefillParams p,
+                           int32_t *walk)
 {
     using L = Layout2<HD>;
+    // SKEW, the K/V protocol: tile c's barrier carries K(c) and V(c-1), with the
+    // K and V slots freed separately, so K(c) is requested a tile period early
+    // (items of many key tiles: the window path, landmark and dilated
+    // patterns); otherwise one K/V stage per tile, freed after the second
+    // head's P V (items of one or two tiles, where a P V product should not
+    // wait for the next tile's K).  See the producer.
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -986,130 +995,198 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int kv_iter = 0, it = 0;
-            int last_k_par[STAGES], last_q_par[2] = {-1, -1};
-            for (int s = 0; s < STAGES; ++s) last_k_par[s] = -1;
-            bool ok = true;
-            // Tile c's barrier (K_FULL slot c % STAGES) carries K(c) and V(c-1): the
-            // K slot is freed after the second head's S (a tile earlier than a
-            // combined K/V stage would be), so K(c) is requested a whole tile
-            // period before S_A(c) needs it, and the MMA warp still waits once per
-            // tile.  The last tile's V rides on the barrier of the tile after it.
-            // pv_*: the previous tile's V, still to be loaded.
-            bool pv_have = false, pv_nar = false;
-            int pv_k0 = 0, pv_kc = 0, pv_z = 0;
-            const CUtensorMap *pv_map = &tmV;
-            // waits until V slot (c_next - 1) % STAGES is free for V(c_next - 1)
-            auto load_prev_v = [&](int c_next) -> bool {
-                const int vc = c_next - 1, vs = vc % STAGES;
-                if (!mbar_wait(BAR(L::V_EMPTY + vs), ((vc / STAGES) & 1) ^ 1, abort_flag, p.status,
-                               p.wait_ns))
-                    return false;
-                return true;
-            };
-            auto issue_prev_v = [&](int c_next, uint32_t bar) {
-                const int vs = (c_next - 1) % STAGES;
-                for (int c = 0; c < HD / 64; ++c)
-                    load_rows<PAT>(sV + vs * L::KB + c * (BN * 128), pv_map, bar, c * 64, pv_kc,
-                                   pv_k0, pv_z);
-            };
-            for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
-                 t = pair_item_rank(blockIdx.x, ++it)) {
-                int b, hp, kvh, qt, cls;
-                decode_level_item<PAT>(t, p, pair_units<QP>(p), b, hp, kvh, qt, cls);
-                int off;
-                const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
-                const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
-                // the item's Q tiles: issued after its first key tile (and the
-                // previous item's last value tile, which the MMA warp needs
-                // first), since their buffers free up only at the previous
-                // item's last S
-                auto load_q_tiles = [&]() -> bool {
-                    for (int x = 0; x < 2; ++x) {
+            if constexpr (!SKEW) {
+                // one stage and one barrier per tile for K and V, freed after the
+                // second head's P V; the Q tiles go first (fixed patterns with
+                // items of one or two key tiles)
+                int kv_iter = 0, it = 0;
+                int last_k_par[STAGES], last_q_par[2] = {-1, -1};
+                for (int s = 0; s < STAGES; ++s) last_k_par[s] = -1;
+                bool ok = true;
+                for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
+                     t = pair_item_rank(blockIdx.x, ++it)) {
+                    int b, hp, kvh, qt, cls;
+                    decode_level_item<PAT>(t, p, pair_units<QP>(p), b, hp, kvh, qt, cls);
+                    int off;
+                    const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
+                    const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
+                    for (int x = 0; x < 2 && ok; ++x) {
                         if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
-                                       p.wait_ns))
-                            return false;
+                                       p.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
                         mbar_expect_tx(BAR(L::Q_FULL + x), L::QB);
                         const int hx = pair_head<QP>(p, kvh, hp, x);
                         const int qrow = QP ? (2 * qt + x) * BM : qt * BM;
                         for (int c = 0; c < HD / 64; ++c)
-                            load_rows<PAT>(sQ + x * L::QB + c * (BM * 128), mq,
-                                           BAR(L::Q_FULL + x), c * 64, cls, qrow, b * p.H + hx);
+                            load_rows<PAT>(sQ + x * L::QB + c * (BM * 128), mq, BAR(L::Q_FULL + x),
+                                           c * 64, cls, qrow, b * p.H + hx);
                         last_q_par[x] = it & 1;
                     }
+                    for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
+                        const int st = kv_iter % STAGES;
+                        const uint32_t ph = (kv_iter / STAGES) & 1;
+                        if (!mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status,
+                                       p.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        const KeyTile kt = key_tile<PAT>(tr, j, p);
+                        const int zkv = b * p.Hkv + kvh;
+                        // landmark tiles: class 0 of the stride-rl view; others: this class
+                        const int kc = kt.land ? 0 : cls;
+                        const bool hi = !PAT || kt.land || cls < p.rem;
+                        if (walk != nullptr)
+                            log_walk(walk, t, b, kvh, hp, qt, cls, kt.k0,
+                                     (kt.full ? 1 : 0) | (kt.land ? 2 : 0));
+                        // test injection: this stage's copies never start, so the MMA
+                        // warp's wait for them runs out (nothing is in flight to drain)
+                        if (p.skip_first_kv && kv_iter == 0) continue;
+                        mbar_expect_tx(BAR(L::K_FULL + st), 2 * L::KB);
+                        for (int c = 0; c < HD / 64; ++c)
+                            load_rows<PAT>(sK + st * L::KB + c * (BN * 128), hi ? &tmK : &tmK2,
+                                           BAR(L::K_FULL + st), c * 64, kc, kt.k0, zkv);
+                        for (int c = 0; c < HD / 64; ++c)
+                            load_rows<PAT>(sV + st * L::KB + c * (BN * 128), hi ? &tmV : &tmV2,
+                                           BAR(L::K_FULL + st), c * 64, kc, kt.k0, zkv);
+                        last_k_par[st] = static_cast<int>(ph);
+                    }
+                }
+                if (!ok) {
+                    for (int s = 0; s < STAGES; ++s)
+                        if (last_k_par[s] >= 0)
+                            mbar_wait(BAR(L::K_FULL + s), last_k_par[s], nullptr, nullptr, TIMEOUT_NS);
+                    for (int x = 0; x < 2; ++x)
+                        if (last_q_par[x] >= 0)
+                            mbar_wait(BAR(L::Q_FULL + x), last_q_par[x], nullptr, nullptr, TIMEOUT_NS);
+                }
+            } else {
+                int kv_iter = 0, it = 0;
+                int last_k_par[STAGES], last_q_par[2] = {-1, -1};
+                for (int s = 0; s < STAGES; ++s) last_k_par[s] = -1;
+                bool ok = true;
+                // Tile c's barrier (K_FULL slot c % STAGES) carries K(c) and V(c-1): the
+                // K slot is freed after the second head's S (a tile earlier than a
+                // combined K/V stage would be), so K(c) is requested a whole tile
+                // period before S_A(c) needs it, and the MMA warp still waits once per
+                // tile.  The last tile's V rides on the barrier of the tile after it.
+                // pv_*: the previous tile's V, still to be loaded.
+                bool pv_have = false, pv_nar = false;
+                int pv_k0 = 0, pv_kc = 0, pv_z = 0;
+                const CUtensorMap *pv_map = &tmV;
+                // waits until V slot (c_next - 1) % STAGES is free for V(c_next - 1)
+                auto load_prev_v = [&](int c_next) -> bool {
+                    const int vc = c_next - 1, vs = vc % STAGES;
+                    if (!mbar_wait(BAR(L::V_EMPTY + vs), ((vc / STAGES) & 1) ^ 1, abort_flag, p.status,
+                                   p.wait_ns))
+                        return false;
                     return true;
                 };
-                for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
+                auto issue_prev_v = [&](int c_next, uint32_t bar) {
+                    const int vs = (c_next - 1) % STAGES;
+                    for (int c = 0; c < HD / 64; ++c)
+                        load_rows<PAT>(sV + vs * L::KB + c * (BN * 128), pv_map, bar, c * 64, pv_kc,
+                                       pv_k0, pv_z);
+                };
+                for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
+                     t = pair_item_rank(blockIdx.x, ++it)) {
+                    int b, hp, kvh, qt, cls;
+                    decode_level_item<PAT>(t, p, pair_units<QP>(p), b, hp, kvh, qt, cls);
+                    int off;
+                    const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
+                    const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
+                    // the item's Q tiles: issued after its first key tile (and the
+                    // previous item's last value tile, which the MMA warp needs
+                    // first), since their buffers free up only at the previous
+                    // item's last S
+                    auto load_q_tiles = [&]() -> bool {
+                        for (int x = 0; x < 2; ++x) {
+                            if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
+                                           p.wait_ns))
+                                return false;
+                            mbar_expect_tx(BAR(L::Q_FULL + x), L::QB);
+                            const int hx = pair_head<QP>(p, kvh, hp, x);
+                            const int qrow = QP ? (2 * qt + x) * BM : qt * BM;
+                            for (int c = 0; c < HD / 64; ++c)
+                                load_rows<PAT>(sQ + x * L::QB + c * (BM * 128), mq,
+                                               BAR(L::Q_FULL + x), c * 64, cls, qrow, b * p.H + hx);
+                            last_q_par[x] = it & 1;
+                        }
+                        return true;
+                    };
+                    for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
+                        const int st = kv_iter % STAGES;
+                        const uint32_t ph = (kv_iter / STAGES) & 1;
+                        if ((pv_have && !load_prev_v(kv_iter)) ||
+                            !mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status,
+                                       p.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        const KeyTile kt = key_tile<PAT>(tr, j, p);
+                        const int zkv = b * p.Hkv + kvh;
+                        // landmark tiles: class 0 of the stride-rl view; others: this class
+                        const int kc = kt.land ? 0 : cls;
+                        const bool hi = !PAT || kt.land || cls < p.rem;
+                        // test injection: this stage's copies never start, so the MMA
+                        // warp's wait for them runs out (nothing is in flight to drain)
+                        if (p.skip_first_kv && kv_iter == 0) {
+                            pv_have = false;
+                            continue;
+                        }
+                        // this tile's K and the previous tile's V complete this tile's
+                        // barrier.  The narrow sink tile is NB_SINK rows at the top of
+                        // each 64-column chunk (the tmK2/tmV2 boxes).
+                        const bool nar = narrow_sink_tile<PAT, NS>(tr, j, p);
+                        if (walk != nullptr)
+                            log_walk(walk, t, b, kvh, hp, qt, cls, kt.k0,
+                                     (kt.full ? 1 : 0) | (kt.land ? 2 : 0) | (nar ? 4 : 0));
+                        const CUtensorMap *mk = nar ? &tmK2 : hi ? &tmK : &tmK2;
+                        const CUtensorMap *mv = nar ? &tmV2 : hi ? &tmV : &tmV2;
+                        const uint32_t kbytes = nar ? 1u * NB_SINK * HD * 2 : L::KB;
+                        const uint32_t vbytes = !pv_have ? 0u : pv_nar ? 1u * NB_SINK * HD * 2 : L::KB;
+                        mbar_expect_tx(BAR(L::K_FULL + st), kbytes + vbytes);
+                        if (pv_have) issue_prev_v(kv_iter, BAR(L::K_FULL + st));
+                        for (int c = 0; c < HD / 64; ++c)
+                            load_rows<PAT>(sK + st * L::KB + c * (BN * 128), mk, BAR(L::K_FULL + st),
+                                           c * 64, kc, kt.k0, zkv);
+                        last_k_par[st] = static_cast<int>(ph);
+                        pv_have = true;
+                        pv_nar = nar;
+                        pv_k0 = kt.k0;
+                        pv_kc = kc;
+                        pv_z = zkv;
+                        pv_map = mv;
+                        if (j == 0 && !load_q_tiles()) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                // the last tile's V, on the barrier of the tile after it
+                if (ok && pv_have) {
                     const int st = kv_iter % STAGES;
                     const uint32_t ph = (kv_iter / STAGES) & 1;
-                    if ((pv_have && !load_prev_v(kv_iter)) ||
-                        !mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status,
-                                   p.wait_ns)) {
+                    // the barrier's previous phase (tile kv_iter - 2) must be complete
+                    // before it is armed again: its K slot release says so
+                    if (!load_prev_v(kv_iter) ||
+                        !mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
-                        break;
-                    }
-                    const KeyTile kt = key_tile<PAT>(tr, j, p);
-                    const int zkv = b * p.Hkv + kvh;
-                    // landmark tiles: class 0 of the stride-rl view; others: this class
-                    const int kc = kt.land ? 0 : cls;
-                    const bool hi = !PAT || kt.land || cls < p.rem;
-                    // test injection: this stage's copies never start, so the MMA
-                    // warp's wait for them runs out (nothing is in flight to drain)
-                    if (p.skip_first_kv && kv_iter == 0) {
-                        pv_have = false;
-                        continue;
-                    }
-                    // this tile's K and the previous tile's V complete this tile's
-                    // barrier.  The narrow sink tile is NB_SINK rows at the top of
-                    // each 64-column chunk (the tmK2/tmV2 boxes).
-                    const bool nar = narrow_sink_tile<PAT, NS>(tr, j, p);
-                    if (p.walk != nullptr)
-                        log_walk(p, t, b, kvh, hp, qt, cls, kt.k0,
-                                 (kt.full ? 1 : 0) | (kt.land ? 2 : 0) | (nar ? 4 : 0));
-                    const CUtensorMap *mk = nar ? &tmK2 : hi ? &tmK : &tmK2;
-                    const CUtensorMap *mv = nar ? &tmV2 : hi ? &tmV : &tmV2;
-                    const uint32_t kbytes = nar ? 1u * NB_SINK * HD * 2 : L::KB;
-                    const uint32_t vbytes = !pv_have ? 0u : pv_nar ? 1u * NB_SINK * HD * 2 : L::KB;
-                    mbar_expect_tx(BAR(L::K_FULL + st), kbytes + vbytes);
-                    if (pv_have) issue_prev_v(kv_iter, BAR(L::K_FULL + st));
-                    for (int c = 0; c < HD / 64; ++c)
-                        load_rows<PAT>(sK + st * L::KB + c * (BN * 128), mk, BAR(L::K_FULL + st),
-                                       c * 64, kc, kt.k0, zkv);
-                    last_k_par[st] = static_cast<int>(ph);
-                    pv_have = true;
-                    pv_nar = nar;
-                    pv_k0 = kt.k0;
-                    pv_kc = kc;
-                    pv_z = zkv;
-                    pv_map = mv;
-                    if (j == 0 && !load_q_tiles()) {
-                        ok = false;
-                        break;
+                    } else {
+                        mbar_expect_tx(BAR(L::K_FULL + st), pv_nar ? 1u * NB_SINK * HD * 2 : L::KB);
+                        issue_prev_v(kv_iter, BAR(L::K_FULL + st));
+                        last_k_par[st] = static_cast<int>(ph);
                     }
                 }
-            }
-            // the last tile's V, on the barrier of the tile after it
-            if (ok && pv_have) {
-                const int st = kv_iter % STAGES;
-                const uint32_t ph = (kv_iter / STAGES) & 1;
-                // the barrier's previous phase (tile kv_iter - 2) must be complete
-                // before it is armed again: its K slot release says so
-                if (!load_prev_v(kv_iter) ||
-                    !mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status, p.wait_ns)) {
-                    ok = false;
-                } else {
-                    mbar_expect_tx(BAR(L::K_FULL + st), pv_nar ? 1u * NB_SINK * HD * 2 : L::KB);
-                    issue_prev_v(kv_iter, BAR(L::K_FULL + st));
-                    last_k_par[st] = static_cast<int>(ph);
+                if (!ok) {
+                    for (int s = 0; s < STAGES; ++s)
+                        if (last_k_par[s] >= 0)
+                            mbar_wait(BAR(L::K_FULL + s), last_k_par[s], nullptr, nullptr, TIMEOUT_NS);
+                    for (int x = 0; x < 2; ++x)
+                        if (last_q_par[x] >= 0)
+                            mbar_wait(BAR(L::Q_FULL + x), last_q_par[x], nullptr, nullptr, TIMEOUT_NS);
                 }
-            }
-            if (!ok) {
-                for (int s = 0; s < STAGES; ++s)
-                    if (last_k_par[s] >= 0)
-                        mbar_wait(BAR(L::K_FULL + s), last_k_par[s], nullptr, nullptr, TIMEOUT_NS);
-                for (int x = 0; x < 2; ++x)
-                    if (last_q_par[x] >= 0)
-                        mbar_wait(BAR(L::Q_FULL + x), last_q_par[x], nullptr, nullptr, TIMEOUT_NS);
             }
         }
     } else if (warp == 1) {
@@ -1147,7 +1224,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     mma_ts_e(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
                 else
                     mma_ts_group8(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
-                if (x == 1) tc_commit_e(BAR(L::V_EMPTY + prev_st));
+                // the V slot (window path) or the whole K/V stage (fixed patterns)
+                if (x == 1) tc_commit_e(BAR((SKEW ? L::V_EMPTY : L::KV_EMPTY) + prev_st));
                 if (prev_last) tc_commit_e(BAR(L::O_FULL + x));
                 // a softmax warpgroup that gave up arrived once more on the barrier
                 // above; the product just issued read a garbage P, which is harmless
@@ -1162,7 +1240,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 mma_ss_group<HD / 16>(s_t, qb, kb, narrow ? idesc_s16 : idesc_s);
                 tc_commit_e(BAR(L::S_FULL + x));
                 if (last) tc_commit_e(BAR(L::Q_EMPTY + x));
-                if (x == 1) tc_commit_e(BAR(L::KV_EMPTY + st));
+                if (SKEW && x == 1) tc_commit_e(BAR(L::KV_EMPTY + st));  // the K slot
             };
             using X0 = std::integral_constant<int, 0>;
             using X1 = std::integral_constant<int, 1>;
@@ -1177,8 +1255,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     const uint32_t ph = (kv_iter / STAGES) & 1;
                     const bool last = (j == tr.count - 1);
                     const bool narrow = narrow_sink_tile<PAT, NS>(tr, j, p);
-                    // K(c) and V(c-1) have landed: one wait per tile
-                    if (!warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, p.wait_ns)) {
+                    // window path: K(c) and V(c-1) have landed (one wait per tile,
+                    // before P_A(c-1) V); fixed patterns: K(c) and V(c), after it
+                    if (SKEW &&
+                        !warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -1187,7 +1267,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         ok = false;
                         break;
                     }
-                    if (j == 0 && !warp_wait(BAR(L::Q_FULL + 0), it & 1, abort_flag, p.status, p.wait_ns)) {
+                    if ((j == 0 &&
+                         !warp_wait(BAR(L::Q_FULL + 0), it & 1, abort_flag, p.status, p.wait_ns)) ||
+                        (!SKEW &&
+                         !warp_wait(BAR(L::K_FULL + st), ph, abort_flag, p.status, p.wait_ns))) {
                         ok = false;
                         break;
                     }
@@ -1213,9 +1296,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     prev_narrow = narrow;
                 }
             }
+            // the last tile's V (window path: on the barrier of the tile after it)
             if (ok && have_prev &&
-                warp_wait(BAR(L::K_FULL + kv_iter % STAGES), (kv_iter / STAGES) & 1, abort_flag,
-                          p.status, p.wait_ns)) {
+                (!SKEW || warp_wait(BAR(L::K_FULL + kv_iter % STAGES), (kv_iter / STAGES) & 1,
+                                    abort_flag, p.status, p.wait_ns))) {
                 if (issue_pv(X0{})) issue_pv(X1{});
             }
             // drain: every MMA this warp issued has completed before exit
@@ -1623,13 +1707,13 @@ bool make_view(CUtensorMap *m, const void *base, uint64_t d, uint64_t R, uint64_
 
 // One launch of the pair kernel: head pairs of an even group, or (QP) pairs of
 // adjacent q tiles of one head for an odd group.
-template <int HD, bool PAT, bool QP, bool NS>
+template <int HD, bool PAT, bool QP, bool NS, bool SKEW = true>
 int launch_pair(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                 const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
-                PrefillParams p, int per_unit, cudaStream_t stream)
+                PrefillParams p, int per_unit, cudaStream_t stream, int32_t *walk)
 {
     using L2 = Layout2<HD>;
-    if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS>>(L2::DYN_SMEM) != cudaSuccess)
+    if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS, SKEW>>(L2::DYN_SMEM) != cudaSuccess)
         return SWA_ERR_CUDA;
     if constexpr (QP) {
         p.n_qt = (p.n + 2 * BM - 1) / (2 * BM);  // levels of q-tile pairs
@@ -1638,15 +1722,15 @@ int launch_pair(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap 
         p.num_items = p.B * p.Hkv * (p.G / 2) * per_unit;
     }
     const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-    swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS>
-        <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
+    swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS, SKEW>
+        <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p, walk);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
 template <int HD, bool PAT>
 int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                    const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
-                   PrefillParams p, int per_unit, cudaStream_t stream)
+                   PrefillParams p, int per_unit, cudaStream_t stream, int32_t *walk)
 {
     if constexpr (!PAT) {
         // the window path: the narrow sink tile is compiled in only where it is
@@ -1654,26 +1738,34 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
         const bool ns = p.g >= 1 && p.g <= NB_SINK;
         if (p.G % 2 == 0)
             return ns ? launch_pair<HD, false, false, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
-                                                            stream)
+                                                            stream, walk)
                       : launch_pair<HD, false, false, false>(mq, mk, mv, mq2, mk2, mv2, p,
-                                                             per_unit, stream);
+                                                             per_unit, stream, walk);
         return ns ? launch_pair<HD, false, true, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
-                                                       stream)
+                                                       stream, walk)
                   : launch_pair<HD, false, true, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
-                                                        stream);
+                                                        stream, walk);
     } else {
         // the fixed patterns: head pairs for even groups, the single-head kernel
-        // for odd ones
-        if (p.G % 2 == 0)
-            return launch_pair<HD, true, false, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
-                                                       stream);
+        // for odd ones.  An item's key tiles number about min(window, class
+        // rows) / BN + 1: the skewed K/V protocol for four tiles' worth and more
+        // (landmarks, dilated windows), one stage per tile below that (the
+        // strided head's short classes).
+        if (p.G % 2 == 0) {
+            const int span = p.w < p.n_hi ? p.w : p.n_hi;
+            if (span >= 4 * BN)
+                return launch_pair<HD, true, false, false, true>(mq, mk, mv, mq2, mk2, mv2, p,
+                                                                 per_unit, stream, walk);
+            return launch_pair<HD, true, false, false, false>(mq, mk, mv, mq2, mk2, mv2, p,
+                                                              per_unit, stream, walk);
+        }
         using L = Layout<HD>;
         if (smem_opt_in<swa_prefill_bf16_sm103<HD, PAT>>(L::DYN_SMEM) != cudaSuccess)
             return SWA_ERR_CUDA;
         p.num_items = p.B * p.H * per_unit;
         const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
         swa_prefill_bf16_sm103<HD, PAT>
-            <<<grid, NTHREADS, L::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p);
+            <<<grid, NTHREADS, L::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p, walk);
         return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
     }
 }
@@ -1681,8 +1773,7 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
 template <int HD>
 int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, const float *sink,
               int B, int H, int Hkv, int n, int n_k, int w, int g, float scale,
-              const int32_t *pos0, int R, int rl, cudaStream_t stream, int32_t *walk,
-              long long walk_cap)
+              const int32_t *pos0, int R, int rl, cudaStream_t stream, int32_t *walk)
 {
     if (rl > 0) R = 1;
     const bool pat = R > 1 || rl > 0;
@@ -1749,10 +1840,8 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     if (p.status == nullptr) return SWA_ERR_CUDA;
     p.wait_ns = TIMEOUT_NS;
     p.skip_first_kv = take_injected_stall(SWA_STALL_PREFILL, &p.wait_ns) ? 1 : 0;
-    p.walk = walk;
-    p.walk_cap = walk_cap;
-    if (pat) return launch_kernels<HD, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream);
-    return launch_kernels<HD, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream);
+    if (pat) return launch_kernels<HD, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream, walk);
+    return launch_kernels<HD, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream, walk);
 }
 
 }  // namespace
@@ -1760,14 +1849,14 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
                         const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
                         int g, float scale, const int32_t *pos0, int R, int rl,
-                        cudaStream_t stream, int32_t *walk, long long walk_cap)
+                        cudaStream_t stream, int32_t *walk)
 {
     if (d == 128)
         return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
-                              stream, walk, walk_cap);
+                              stream, walk);
     if (d == 64)
         return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
-                             stream, walk, walk_cap);
+                             stream, walk);
     return SWA_ERR_UNSUPPORTED;
 }
 

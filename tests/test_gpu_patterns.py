@@ -31,6 +31,10 @@ CASES = [
     # 128 rows (two q tiles for some, one for the others)
     ("strided", 8, 16, 16, 644, 64, 0, 0, 5),       # single-head kernel
     ("dilated", 4, 32, 16, 1283, 64, 30, 0, 10),    # head pairs
+    # items of four key tiles and more (window and class rows >= 512): the head-pair
+    # kernel's skewed key/value protocol under the fixed patterns
+    ("landmark", 1, 4, 2, 2100, 128, 600, 4, 32),
+    ("dilated", 1, 4, 2, 2230, 128, 700, 0, 2),     # classes of 1115 rows
 ]
 
 

@@ -92,8 +92,9 @@ def test_window_walk_matches_oracle_tiles(swa, oracle_mod, B, H, Hkv, n, d, w, g
 
 
 @pytest.mark.gpu
-def test_landmark_walk_matches_oracle_mask(swa, oracle_mod):
-    B, H, Hkv, n, d, w, g, r = 1, 4, 2, 1500, 128, 256, 4, 16
+@pytest.mark.parametrize("n,w,g,r", [(1500, 256, 4, 16), (2100, 600, 4, 32)])
+def test_landmark_walk_matches_oracle_mask(swa, oracle_mod, n, w, g, r):
+    B, H, Hkv, d = 1, 4, 2, 128
     x = synthetic.prefill_inputs(B, H, Hkv, n, d, w, g, dtype="bf16", seed=3, sink_scale=4.0,
                                  device="cuda")
     out, entries = swa.prefill_walk(x.Q, x.K, x.V, "landmark", w, g, r, x.scale)
