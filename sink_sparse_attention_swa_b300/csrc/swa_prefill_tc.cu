@@ -120,9 +120,11 @@ struct PrefillParams {
 // residue class, the tile's first key index, and flags (1 full, 2 landmark
 // tile, 4 narrow sink tile).  log[0] counts the entries, log[2..3] holds the
 // capacity (a 64-bit count of entries); entry e is at log[WALK_HDR +
-// WALK_ENTRY * e].  The log is a kernel argument of its own, null for every
-// launch but swa_debug_prefill_walk's, kept out of PrefillParams (a larger
-// parameter block made the control warpgroup spill).
+// WALK_ENTRY * e].  The log is a kernel argument of its own, kept out of
+// PrefillParams (a larger parameter block made the control warpgroup spill),
+// and the producers write it only in the WALK instantiations that
+// swa_debug_prefill_walk launches: a per-tile check for a null log cost the
+// product kernels up to 2% on short items.
 constexpr int WALK_HDR = 8, WALK_ENTRY = 8;
 __device__ __forceinline__ void log_walk(int32_t *log, int t, int b, int kvh, int u, int qt, int cls,
                                          int k0, int flags)
@@ -377,7 +379,7 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap *map, 
         tma_load_3d(dst, map, bar, x, row, z);
 }
 
-template <int HD, bool PAT>
+template <int HD, bool PAT, bool WALK>
 __global__ void __launch_bounds__(NTHREADS, 1)
     swa_prefill_bf16_sm103(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK,
@@ -478,7 +480,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // landmark tiles: class 0 of the stride-rl view; others: this class
                     const int kc = kt.land ? 0 : cls;
                     const bool hi = !PAT || kt.land || cls < p.rem;
-                    if (walk != nullptr)
+                    if constexpr (WALK)
                         log_walk(walk, t, b, kvh, hg, qt, cls, kt.k0,
                                  (kt.full ? 1 : 0) | (kt.land ? 2 : 0));
                     // test injection: this stage's copies never start, so the MMA
@@ -924,7 +926,7 @@ __device__ __forceinline__ void softmax_half(const uint32_t (&sa)[32], const uin
     }
 }
 
-template <int HD, bool PAT, bool QP, bool NS, bool SKEW>
+template <int HD, bool PAT, bool QP, bool NS, bool SKEW, bool WALK>
 __global__ void __launch_bounds__(NTHREADS2, 1)
     swa_prefill_bf16_pair_sm103(const __grid_constant__ CUtensorMap tmQ,
                                 const __grid_constant__ CUtensorMap tmK,
@@ -1037,7 +1039,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         // landmark tiles: class 0 of the stride-rl view; others: this class
                         const int kc = kt.land ? 0 : cls;
                         const bool hi = !PAT || kt.land || cls < p.rem;
-                        if (walk != nullptr)
+                        if constexpr (WALK)
                             log_walk(walk, t, b, kvh, hp, qt, cls, kt.k0,
                                      (kt.full ? 1 : 0) | (kt.land ? 2 : 0));
                         // test injection: this stage's copies never start, so the MMA
@@ -1096,10 +1098,14 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     int off;
                     const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
                     const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
-                    // the item's Q tiles: issued after its first key tile (and the
-                    // previous item's last value tile, which the MMA warp needs
-                    // first), since their buffers free up only at the previous
-                    // item's last S
+                    // the item's Q tiles.  Their buffers free up only at the
+                    // previous item's last S, and the MMA warp first needs the
+                    // previous item's last value tile, so on the plain window path
+                    // they go after the item's first key tile (which carries that
+                    // V).  Where the first key tile is the narrow sink tile, and
+                    // for the fixed patterns, they go first: measured 1.5% (sinks)
+                    // and 2-4% (patterns) faster that way, the other order 1-4%
+                    // faster without sinks.
                     auto load_q_tiles = [&]() -> bool {
                         for (int x = 0; x < 2; ++x) {
                             if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
@@ -1115,6 +1121,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         }
                         return true;
                     };
+                    if ((PAT || NS) && !load_q_tiles()) ok = false;
                     for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
                         const int st = kv_iter % STAGES;
                         const uint32_t ph = (kv_iter / STAGES) & 1;
@@ -1139,7 +1146,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         // barrier.  The narrow sink tile is NB_SINK rows at the top of
                         // each 64-column chunk (the tmK2/tmV2 boxes).
                         const bool nar = narrow_sink_tile<PAT, NS>(tr, j, p);
-                        if (walk != nullptr)
+                        if constexpr (WALK)
                             log_walk(walk, t, b, kvh, hp, qt, cls, kt.k0,
                                      (kt.full ? 1 : 0) | (kt.land ? 2 : 0) | (nar ? 4 : 0));
                         const CUtensorMap *mk = nar ? &tmK2 : hi ? &tmK : &tmK2;
@@ -1158,7 +1165,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         pv_kc = kc;
                         pv_z = zkv;
                         pv_map = mv;
-                        if (j == 0 && !load_q_tiles()) {
+                        if (!PAT && !NS && j == 0 && !load_q_tiles()) {
                             ok = false;
                             break;
                         }
@@ -1707,13 +1714,14 @@ bool make_view(CUtensorMap *m, const void *base, uint64_t d, uint64_t R, uint64_
 
 // One launch of the pair kernel: head pairs of an even group, or (QP) pairs of
 // adjacent q tiles of one head for an odd group.
-template <int HD, bool PAT, bool QP, bool NS, bool SKEW = true>
+template <int HD, bool WALK, bool PAT, bool QP, bool NS, bool SKEW = true>
 int launch_pair(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                 const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
                 PrefillParams p, int per_unit, cudaStream_t stream, int32_t *walk)
 {
     using L2 = Layout2<HD>;
-    if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS, SKEW>>(L2::DYN_SMEM) != cudaSuccess)
+    if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS, SKEW, WALK>>(L2::DYN_SMEM) !=
+        cudaSuccess)
         return SWA_ERR_CUDA;
     if constexpr (QP) {
         p.n_qt = (p.n + 2 * BM - 1) / (2 * BM);  // levels of q-tile pairs
@@ -1722,29 +1730,30 @@ int launch_pair(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap 
         p.num_items = p.B * p.Hkv * (p.G / 2) * per_unit;
     }
     const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-    swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS, SKEW>
+    swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS, SKEW, WALK>
         <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p, walk);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
-template <int HD, bool PAT>
+template <int HD, bool WALK, bool PAT>
 int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                    const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
                    PrefillParams p, int per_unit, cudaStream_t stream, int32_t *walk)
 {
+    // pair<QP, NS, SKEW>(): one launch of that pair-kernel instantiation
+    auto pair = [&](auto qp, auto ns, auto skew) {
+        return launch_pair<HD, WALK, PAT, decltype(qp)::value, decltype(ns)::value,
+                           decltype(skew)::value>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream,
+                                                  walk);
+    };
+    using T = std::true_type;
+    using F = std::false_type;
     if constexpr (!PAT) {
         // the window path: the narrow sink tile is compiled in only where it is
         // used (1 <= g <= NB_SINK); an odd group pairs adjacent q tiles of one head
         const bool ns = p.g >= 1 && p.g <= NB_SINK;
-        if (p.G % 2 == 0)
-            return ns ? launch_pair<HD, false, false, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
-                                                            stream, walk)
-                      : launch_pair<HD, false, false, false>(mq, mk, mv, mq2, mk2, mv2, p,
-                                                             per_unit, stream, walk);
-        return ns ? launch_pair<HD, false, true, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
-                                                       stream, walk)
-                  : launch_pair<HD, false, true, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit,
-                                                        stream, walk);
+        if (p.G % 2 == 0) return ns ? pair(F{}, T{}, T{}) : pair(F{}, F{}, T{});
+        return ns ? pair(T{}, T{}, T{}) : pair(T{}, F{}, T{});
     } else {
         // the fixed patterns: head pairs for even groups, the single-head kernel
         // for odd ones.  An item's key tiles number about min(window, class
@@ -1753,18 +1762,14 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
         // strided head's short classes).
         if (p.G % 2 == 0) {
             const int span = p.w < p.n_hi ? p.w : p.n_hi;
-            if (span >= 4 * BN)
-                return launch_pair<HD, true, false, false, true>(mq, mk, mv, mq2, mk2, mv2, p,
-                                                                 per_unit, stream, walk);
-            return launch_pair<HD, true, false, false, false>(mq, mk, mv, mq2, mk2, mv2, p,
-                                                              per_unit, stream, walk);
+            return span >= 4 * BN ? pair(F{}, F{}, T{}) : pair(F{}, F{}, F{});
         }
         using L = Layout<HD>;
-        if (smem_opt_in<swa_prefill_bf16_sm103<HD, PAT>>(L::DYN_SMEM) != cudaSuccess)
+        if (smem_opt_in<swa_prefill_bf16_sm103<HD, PAT, WALK>>(L::DYN_SMEM) != cudaSuccess)
             return SWA_ERR_CUDA;
         p.num_items = p.B * p.H * per_unit;
         const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-        swa_prefill_bf16_sm103<HD, PAT>
+        swa_prefill_bf16_sm103<HD, PAT, WALK>
             <<<grid, NTHREADS, L::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p, walk);
         return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
     }
@@ -1840,8 +1845,16 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     if (p.status == nullptr) return SWA_ERR_CUDA;
     p.wait_ns = TIMEOUT_NS;
     p.skip_first_kv = take_injected_stall(SWA_STALL_PREFILL, &p.wait_ns) ? 1 : 0;
-    if (pat) return launch_kernels<HD, true>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream, walk);
-    return launch_kernels<HD, false>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream, walk);
+    // the logged walk is a kernel of its own, so the product kernels carry no
+    // per-tile check for it
+    auto launch = [&](auto walk_on, auto pat_on) {
+        return launch_kernels<HD, decltype(walk_on)::value, decltype(pat_on)::value>(
+            mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream, walk);
+    };
+    using T = std::true_type;
+    using F = std::false_type;
+    if (walk != nullptr) return pat ? launch(T{}, T{}) : launch(T{}, F{});
+    return pat ? launch(F{}, T{}) : launch(F{}, F{});
 }
 
 }  // namespace
