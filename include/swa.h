@@ -370,6 +370,22 @@ int swa_debug_prefill_walk(const void *Q, const void *K, const void *V, void *O,
                            float scale, int32_t *log, int64_t log_entries, swa_stream_t stream);
 
 /*
+ * swa_debug_prefill_cta_pairs -- an alternative kernel for swa_prefill_ex
+ * (bf16, window path) with no counterpart on the pages: the tile loop of the
+ * default kernel on clusters of two CTAs that share each tensor-core MMA
+ * (tcgen05 cta_group::2, M = 256), so that each SM reads half of the K and V
+ * operands.  It computes the same output (and LSE, if lse is not null) as
+ * swa_prefill_ex; it measured slower than the default kernel on this build's
+ * workloads and is kept as a tested alternative, not used by the other entry
+ * points.  Arguments, layouts and errors as swa_prefill_ex (dtype bf16), plus
+ * SWA_ERR_UNSUPPORTED unless d == 128, H / Hkv is even, H % 4 == 0 and g is 0
+ * or above 16.
+ */
+int swa_debug_prefill_cta_pairs(const void *Q, const void *K, const void *V, void *O, float *lse,
+                                int B, int H, int Hkv, int n, int d, int w, int g, float scale,
+                                swa_stream_t stream);
+
+/*
  * swa_debug_inject_stall -- a test aid with no counterpart on the pages; it
  * lets a test run the kernels' timeout path without faulting or hanging the
  * GPU.  The next launch of the chosen kind on the current device leaves out

@@ -68,6 +68,7 @@ SIGNATURES = {
     "swa_get_device_status": (_i, [_p]),
     "swa_debug_inject_stall": (_i, [_i, _i64]),
     "swa_debug_prefill_walk": (_i, [_p] * 4 + [_i] * 5 + [_i] * 4 + [_f, _p, _i64, _p]),
+    "swa_debug_prefill_cta_pairs": (_i, [_p, _p, _p, _p, _p] + [_i] * 7 + [_f, _p]),
     "swa_status_string": (ctypes.c_char_p, [_i]),
     "swa_version": (_i, []),
     "swa_selftest_umma": (_i, [_p, _p, _p, _p, _p, _p]),
@@ -353,6 +354,30 @@ def device_status(stream=None) -> int:
 
 
 WALK_FIELDS = ("item", "b", "kvh", "unit", "qtile", "cls", "k0", "flags")
+
+
+def prefill_cta_pairs(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None,
+                      lse=None, stream=None):
+    """The bf16 window-path prefill on the CTA-pair kernel
+    (swa_debug_prefill_cta_pairs): same arguments and result as prefill();
+    raises SwaError (SWA_ERR_UNSUPPORTED) unless d == 128, H / Hkv is even,
+    H % 4 == 0 and g is 0 or above 16."""
+    _need(q, "q", torch.bfloat16)
+    B, H, n, d = q.shape
+    Hkv = k.shape[1]
+    _need(k, "k", torch.bfloat16, (B, Hkv, n, d))
+    _need(v, "v", torch.bfloat16, (B, Hkv, n, d))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, n))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = _load().swa_debug_prefill_cta_pairs(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                             Hkv, n, d, int(w), int(g), scale,
+                                             _stream(stream, q.device))
+    _check("swa_debug_prefill_cta_pairs", rc)
+    return out
 
 
 def prefill_walk(q, k, v, pattern: str, w: int, g: int = 0, r: int = 1,

@@ -192,6 +192,20 @@ int swa_debug_prefill_walk(const void *Q, const void *K, const void *V, void *O,
                                 scale, SWA_BF16, stream, log);
 }
 
+int swa_debug_prefill_cta_pairs(const void *Q, const void *K, const void *V, void *O, float *lse,
+                                int B, int H, int Hkv, int n, int d, int w, int g, float scale,
+                                swa_stream_t stream)
+{
+    int rc = check_heads(B, H, Hkv, d, w, g);
+    if (rc != SWA_OK) return rc;
+    if (n < 1 || n > INT32_MAX - 256 || !scale_ok(scale)) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SWA_ERR_INVALID_ARG;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H * ((n + 127) / 128) > INT32_MAX) return SWA_ERR_INVALID_ARG;
+    return launch_prefill_bf16(Q, K, V, O, lse, nullptr, B, H, Hkv, n, n, d, w, g, scale, nullptr,
+                               1, 0, reinterpret_cast<cudaStream_t>(stream), nullptr, true);
+}
+
 size_t swa_prefill_chunk_workspace_bytes(int B, int Hkv, int T, int d, int w, int g,
                                          swa_dtype dtype)
 {

@@ -238,11 +238,12 @@ cudaError_t smem_opt_in(int bytes)
 //           pos0 == null.
 // walk: a diagnostic log of the key tiles the kernels load (the layout of
 // swa_debug_prefill_walk, its capacity in its header), or null for a plain
-// launch.
+// launch.  cta_pairs: run the window path on the CTA-pair kernel
+// (swa_debug_prefill_cta_pairs; SWA_ERR_UNSUPPORTED where it does not apply).
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
                         const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
                         int g, float scale, const int32_t *pos0, int R, int rl,
-                        cudaStream_t stream, int32_t *walk = nullptr);
+                        cudaStream_t stream, int32_t *walk = nullptr, bool cta_pairs = false);
 int launch_prefill_f32(const void *Q, const void *K, const void *V, void *O, float *lse,
                        const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
                        int g, float scale, const int32_t *pos0, int R, int rl,

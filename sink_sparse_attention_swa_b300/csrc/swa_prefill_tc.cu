@@ -304,8 +304,9 @@ __device__ __forceinline__ void store_o_rows(uint32_t o_addr, float inv_l,
 // each round loads 32 columns of O from tensor memory, scales and rounds them,
 // turns them around in `stage` and stores them.  Once the last round's load
 // has completed the warp arrives on `empty_bar` (the O columns may be
-// overwritten), before that round's stores.
-template <int HD>
+// overwritten), before that round's stores; with CLUSTER, `empty_bar` is a
+// shared::cluster address (a barrier of either CTA of a pair).
+template <int HD, bool CLUSTER = false>
 __device__ __forceinline__ void store_o_rows_chunked(uint32_t o_addr, float inv_l,
                                                      __nv_bfloat16 *orow, bool row_ok,
                                                      uint8_t *stage, int lane, uint32_t empty_bar)
@@ -329,7 +330,12 @@ __device__ __forceinline__ void store_o_rows_chunked(uint32_t o_addr, float inv_
         if (q == HD / 32 - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar);
+            if (lane == 0) {
+                if constexpr (CLUSTER)
+                    mbar_arrive_cluster(empty_bar);  // a shared::cluster address
+                else
+                    mbar_arrive(empty_bar);
+            }
         }
 #pragma unroll
         for (int v = 0; v < 4; ++v)
@@ -1712,6 +1718,51 @@ bool make_view(CUtensorMap *m, const void *base, uint64_t d, uint64_t R, uint64_
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The window path on CTA pairs (cta_group::2): see swa_prefill_duo.cuh.
+#include "swa_prefill_duo.cuh"
+
+// Clusters of two CTAs of the CTA-pair kernel that fit on the device at once
+// (0 if it cannot run), worked out once per device.
+template <int HD, bool SHARED>
+int duo_clusters()
+{
+    static std::atomic<int> known[kMaxDevices];  // 0: not yet known; else clusters + 1
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    const int k = known[dev].load(std::memory_order_acquire);
+    if (k > 0) return k - 1;
+    using L = LayoutD<HD, SHARED>;
+    int n = 0;
+    if (smem_opt_in<swa_prefill_bf16_duo_sm103<HD, SHARED>>(L::DYN_SMEM) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms() / 2));
+        cfg.blockDim = dim3(NTHREADS2);
+        cfg.dynamicSmemBytes = L::DYN_SMEM;
+        if (cudaOccupancyMaxActiveClusters(&n, swa_prefill_bf16_duo_sm103<HD, SHARED>, &cfg) !=
+            cudaSuccess)
+            n = 0;
+    }
+    (void)cudaGetLastError();  // a refusal above is an answer, not an error to keep
+    known[dev].store(n + 1, std::memory_order_release);
+    return n;
+}
+
+// One launch of the CTA-pair kernel (window path, even group, H % 4 == 0);
+// SWA_ERR_UNSUPPORTED if no cluster of two fits.
+template <int HD, bool SHARED>
+int launch_duo(const CUtensorMap &mq, const CUtensorMap &mkh, const CUtensorMap &mv,
+               PrefillParams p, cudaStream_t stream)
+{
+    using L = LayoutD<HD, SHARED>;
+    const int fit = duo_clusters<HD, SHARED>();
+    if (fit <= 0) return SWA_ERR_UNSUPPORTED;
+    p.num_items = p.B * (p.H / 4) * p.n_qt;
+    const int clusters = p.num_items < fit ? p.num_items : fit;
+    swa_prefill_bf16_duo_sm103<HD, SHARED>
+        <<<2 * clusters, NTHREADS2, L::DYN_SMEM, stream>>>(mq, mkh, mv, p);
+    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
 // One launch of the pair kernel: head pairs of an even group, or (QP) pairs of
 // adjacent q tiles of one head for an odd group.
 template <int HD, bool WALK, bool PAT, bool QP, bool NS, bool SKEW = true>
@@ -1778,7 +1829,8 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
 template <int HD>
 int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, const float *sink,
               int B, int H, int Hkv, int n, int n_k, int w, int g, float scale,
-              const int32_t *pos0, int R, int rl, cudaStream_t stream, int32_t *walk)
+              const int32_t *pos0, int R, int rl, cudaStream_t stream, int32_t *walk,
+              bool cta_pairs)
 {
     if (rl > 0) R = 1;
     const bool pat = R > 1 || rl > 0;
@@ -1847,6 +1899,21 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     p.skip_first_kv = take_injected_stall(SWA_STALL_PREFILL, &p.wait_ns) ? 1 : 0;
     // the logged walk is a kernel of its own, so the product kernels carry no
     // per-tile check for it
+    // the window path on CTA pairs, on request only (it measured 4-9% slower
+    // than the pair kernel on the Mistral-like, Gemma-3-like and long layers):
+    // d = 128, an even group, heads in quads, no narrow sink tile
+    if (cta_pairs) {
+        if constexpr (HD == 128) {
+            if (!pat && walk == nullptr && p.G % 2 == 0 && H % 4 == 0 &&
+                !(g >= 1 && g <= NB_SINK)) {
+                CUtensorMap mkh;
+                if (!make_map_3d(&mkh, K, HD, n_k, ZK, BN / 2)) return SWA_ERR_CUDA;
+                return p.G % 4 == 0 ? launch_duo<HD, true>(mq, mkh, mv, p, stream)
+                                    : launch_duo<HD, false>(mq, mkh, mv, p, stream);
+            }
+        }
+        return SWA_ERR_UNSUPPORTED;
+    }
     auto launch = [&](auto walk_on, auto pat_on) {
         return launch_kernels<HD, decltype(walk_on)::value, decltype(pat_on)::value>(
             mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream, walk);
@@ -1862,14 +1929,14 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
 int launch_prefill_bf16(const void *Q, const void *K, const void *V, void *O, float *lse,
                         const float *sink, int B, int H, int Hkv, int n, int n_k, int d, int w,
                         int g, float scale, const int32_t *pos0, int R, int rl,
-                        cudaStream_t stream, int32_t *walk)
+                        cudaStream_t stream, int32_t *walk, bool cta_pairs)
 {
     if (d == 128)
         return launch_hd<128>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
-                              stream, walk);
+                              stream, walk, cta_pairs);
     if (d == 64)
         return launch_hd<64>(Q, K, V, O, lse, sink, B, H, Hkv, n, n_k, w, g, scale, pos0, R, rl,
-                             stream, walk);
+                             stream, walk, cta_pairs);
     return SWA_ERR_UNSUPPORTED;
 }
 

@@ -393,5 +393,171 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+
+// ------------------------------------------------------------------ CTA pairs
+// Two CTAs of a cluster of two sharing one tcgen05 MMA (cta_group::2): the
+// MMA of M = 256 rows takes rows 0-127 of A from the even CTA's shared (or
+// tensor) memory and rows 128-255 from the odd CTA's, splits B along N between
+// the two (each CTA holds N/2 of its rows, at the same shared-memory offset)
+// and writes each CTA's 128 rows of D into that CTA's tensor memory.  Every
+// tcgen05 instruction of such a kernel names cta_group::2.
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of shared-memory address `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// One arrival on an mbarrier given by its shared::cluster address (this CTA's
+// or the peer's).  The arrivals that cross the pair follow a completed
+// tensor-memory store (tcgen05.wait::st, then tcgen05.fence::before_thread_sync)
+// or a completed tensor-memory load, so they need no cluster-scope release;
+// with .release.cluster (and .acquire.cluster on the waiting side) the
+// pair kernel's hand-offs took 1.3x as long.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_bar)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait for a barrier that the peer CTA's threads or copies also complete;
+// the same bound and error reporting.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                  int *status, uint64_t timeout_ns)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                if (abort != nullptr) *abort = 1;
+                if (status != nullptr) atomicOr(status, 1);
+                return false;
+            }
+        }
+    }
+}
+
+// Every thread of both CTAs: arrive, then wait for all the others (the
+// per-thread form: a warp need not be converged).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\t"
+                 "barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// 3-D tiled load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (its shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t cl_bar, int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cl_bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// Tensor memory of a CTA pair: one warp of each CTA allocates (the same
+// columns in both) and frees.
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// One arrival on the mbarrier at shared-memory offset `bar` of each CTA in
+// `mask` (bit r: cluster rank r) once every MMA issued before has completed;
+// issued by one elected lane of the calling warp.
+__device__ __forceinline__ void tc_commit2_mc(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+// S = A * B^T over K = 128 for a CTA pair (M = 256): A K-major in 64-column
+// chunks of 128 rows (16 KB apart), B K-major in 64-column chunks of the
+// CTA's N/2 = 64 rows (8 KB apart); k-step ks adds (ks & 3) * 32 bytes within
+// a chunk.  Descriptor start addresses are in 16-byte units.
+__device__ __forceinline__ void mma2_ss_group8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc)
+{
+    const uint32_t al = static_cast<uint32_t>(a), ah = static_cast<uint32_t>(a >> 32);
+    const uint32_t bl = static_cast<uint32_t>(b), bh = static_cast<uint32_t>(b >> 32);
+#define SWA_MMA2_SS(AO, BO) \
+    "add.u32 xl, %1, " #AO ";\n\tadd.u32 yl, %3, " #BO ";\n\t" \
+    "mov.b64 xd, {xl, %2};\n\tmov.b64 yd, {yl, %4};\n\t" \
+    "@e tcgen05.mma.cta_group::2.kind::f16 [%0], xd, yd, %5, t;\n\t"
+    asm volatile("{\n\t.reg .pred e, f, t;\n\t.reg .b32 xl, yl;\n\t.reg .b64 xd, yd;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "setp.ne.b32 f, %5, %5;\n\tsetp.eq.b32 t, %5, %5;\n\t"
+                 "mov.b64 xd, {%1, %2};\n\tmov.b64 yd, {%3, %4};\n\t"
+                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], xd, yd, %5, f;\n\t"
+                 SWA_MMA2_SS(2, 2) SWA_MMA2_SS(4, 4) SWA_MMA2_SS(6, 6) SWA_MMA2_SS(1024, 512)
+                 SWA_MMA2_SS(1026, 514) SWA_MMA2_SS(1028, 516) SWA_MMA2_SS(1030, 518) "}\n" ::"r"(d),
+                 "r"(al), "r"(ah), "r"(bl), "r"(bh), "r"(idesc)
+                 : "memory");
+#undef SWA_MMA2_SS
+}
+
+// O (+)= P * V over K = 128 keys for a CTA pair: P in each CTA's tensor memory
+// (8 columns per k-step), V N-major in shared memory, the CTA's N/2 = 64
+// columns (k-step ks adds ks * 16 rows * 128 B).
+__device__ __forceinline__ void mma2_ts_group8(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                               uint32_t idesc, uint32_t acc0)
+{
+    const uint32_t bl = static_cast<uint32_t>(b), bh = static_cast<uint32_t>(b >> 32);
+#define SWA_MMA2_TS(AO, BO) \
+    "add.u32 ta, %1, " #AO ";\n\tadd.u32 yl, %2, " #BO ";\n\tmov.b64 yd, {yl, %3};\n\t" \
+    "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], yd, %4, t;\n\t"
+    asm volatile("{\n\t.reg .pred e, f, t;\n\t.reg .b32 ta, yl;\n\t.reg .b64 yd;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "setp.ne.b32 f, %5, 0;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+                 "mov.b64 yd, {%2, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], yd, %4, f;\n\t"
+                 SWA_MMA2_TS(8, 128) SWA_MMA2_TS(16, 256) SWA_MMA2_TS(24, 384) SWA_MMA2_TS(32, 512)
+                 SWA_MMA2_TS(40, 640) SWA_MMA2_TS(48, 768) SWA_MMA2_TS(56, 896) "}\n" ::"r"(d),
+                 "r"(a_tmem), "r"(bl), "r"(bh), "r"(idesc), "r"(acc0)
+                 : "memory");
+#undef SWA_MMA2_TS
+}
+
 }  // namespace ptx
 }  // namespace swa
