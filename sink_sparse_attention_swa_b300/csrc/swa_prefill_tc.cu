@@ -823,7 +823,10 @@ __device__ __forceinline__ bool narrow_sink_tile(const TileRange &tr, int j, con
     return j == 0 && tr.ns == 1 && p.g <= NB_SINK;
 }
 // named barriers 1 (head A) and 2 (head B): a softmax warpgroup's 128 threads
-// arrive when P is in tensor memory, the 32 threads of the MMA warp wait
+// arrive when all of P is in tensor memory, the 32 threads of the MMA warp
+// wait; 3 (A) and 4 (B) likewise when P's first 64 keys are (the pair kernel
+// hands P over in two halves, so that the first half's P V runs while the
+// second half is exponentiated)
 constexpr int P_BAR_THREADS = 128 + 32;
 // registers per thread after the hand-over: 128 * (80 + 176 + 176 + 80)
 // equals the 512 * 128 registers the kernel is launched with
@@ -882,6 +885,14 @@ __device__ __forceinline__ void p_arrive(int x)
         asm volatile("bar.arrive 1, %0;" ::"n"(128 + 32) : "memory");
     else
         asm volatile("bar.arrive 2, %0;" ::"n"(128 + 32) : "memory");
+}
+// ... and its first 64 keys (pair kernel)
+__device__ __forceinline__ void p_arrive_half(int x)
+{
+    if (x == 0)
+        asm volatile("bar.arrive 3, %0;" ::"n"(128 + 32) : "memory");
+    else
+        asm volatile("bar.arrive 4, %0;" ::"n"(128 + 32) : "memory");
 }
 
 __device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi)
@@ -1226,17 +1237,22 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 // mbarrier).  A warpgroup that gives up arrives once more and sets
                 // the abort flag, which is checked after every meeting, so this
                 // never waits for an arrival that will not come.
-                asm volatile("bar.sync %0, %1;" ::"n"(1 + x), "n"(P_BAR_THREADS) : "memory");
+                // P_X's first 64 keys: their half of P V goes to the tensor core
+                // while the softmax warpgroup exponentiates the other half
+                asm volatile("bar.sync %0, %1;" ::"n"(3 + x), "n"(P_BAR_THREADS) : "memory");
                 if (prev_first && !warp_wait(BAR(L::O_EMPTY + x), (prev_it & 1) ^ 1, abort_flag,
                                              p.status, p.wait_ns))
                     return false;
                 tc_fence_after();
                 const uint64_t vb = smem_desc_sw128(sV + prev_st * L::KB, BN * 128, 1024);
                 const uint32_t o_t = tmem + x * 256, p_t = tmem + x * 256 + 128;
+                if (!prev_narrow) mma_ts_group4(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
+                asm volatile("bar.sync %0, %1;" ::"n"(1 + x), "n"(P_BAR_THREADS) : "memory");
+                tc_fence_after();
                 if (prev_narrow)  // the narrow sink tile: one K-step of 16 keys
                     mma_ts_e(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
-                else
-                    mma_ts_group8(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
+                else  // keys 64..127: P columns 32.., V rows 64.. (64 * 128 B >> 4)
+                    mma_ts_group4(o_t, p_t + 32, vb + 512, idesc_o, 1u);
                 // the V slot (window path) or the whole K/V stage (fixed patterns)
                 if (x == 1) tc_commit_e(BAR((SKEW ? L::V_EMPTY : L::KV_EMPTY) + prev_st));
                 if (prev_last) tc_commit_e(BAR(L::O_FULL + x));
@@ -1401,6 +1417,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
+                    p_arrive_half(x);
                     p_arrive(x);
                     continue;
                 }
@@ -1482,8 +1499,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 const uint64_t negm2 = pack2(__float_as_uint(-m_use), __float_as_uint(-m_use));
                 uint64_t acc2 = 0;  // two fp32 zeros
                 uint32_t pk[32];
+                // keys 0..63, handed over first, then keys 64..127
                 softmax_half(s[0], s[1], sl2x2, negm2, acc2, pk);
                 tmem_st32(s_addr, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                p_arrive_half(x);
                 softmax_half(s[2], s[3], sl2x2, negm2, acc2, pk);
                 tmem_st32(s_addr + 32, pk);
                 float a0, a1;
@@ -1507,11 +1529,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             ++it;
             t = t_next;
         }
-        // gave up (a wait ran out): one more arrival lets an issuer that is
-        // already waiting for this head's P meet, see the abort flag and stop
+        // gave up (a wait ran out): one more arrival on each of this head's
+        // two P barriers lets an issuer that is already waiting on either meet,
+        // see the abort flag and stop
         if (!ok) {
             *abort_flag = 1;
             __syncwarp();
+            p_arrive_half(x);
             p_arrive(x);
         }
     } else {

@@ -286,6 +286,27 @@ __device__ __forceinline__ void mma_ts_group8(uint32_t d, uint32_t a_tmem, uint6
 #undef SWA_MMA_TS
 }
 
+// Half of mma_ts_group8: O (+)= P * V over 64 keys, four k-steps from the
+// given P columns and V rows (the first four of a 128-key tile, or with
+// a_tmem + 32 and the V descriptor advanced 64 rows, the last four).
+__device__ __forceinline__ void mma_ts_group4(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                              uint32_t acc0)
+{
+    const uint32_t bl = static_cast<uint32_t>(b), bh = static_cast<uint32_t>(b >> 32);
+#define SWA_MMA_TS(AO, BO) \
+    "add.u32 ta, %1, " #AO ";\n\tadd.u32 yl, %2, " #BO ";\n\tmov.b64 yd, {yl, %3};\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yd, %4, t;\n\t"
+    asm volatile("{\n\t.reg .pred e, f, t;\n\t.reg .b32 ta, yl;\n\t.reg .b64 yd;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "setp.ne.b32 f, %5, 0;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+                 "mov.b64 yd, {%2, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], yd, %4, f;\n\t"
+                 SWA_MMA_TS(8, 128) SWA_MMA_TS(16, 256) SWA_MMA_TS(24, 384) "}\n" ::"r"(d),
+                 "r"(a_tmem), "r"(bl), "r"(bh), "r"(idesc), "r"(acc0)
+                 : "memory");
+#undef SWA_MMA_TS
+}
+
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major,
 // B K-major (b_mn_major = 0) or N-major (1), shape M x N.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
