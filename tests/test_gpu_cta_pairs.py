@@ -69,3 +69,25 @@ def test_cta_pairs_refuses_other_shapes(swa, H, Hkv, d, g):
         swa.prefill_cta_pairs(x.Q, x.K, x.V, 64, g, x.scale)
     assert e.value.status == -2
     assert swa.device_status() == 0
+
+
+@pytest.mark.gpu
+def test_cta_pairs_wait_runs_out_and_recovers(swa, oracle_mod):
+    """The bounded-wait path of the CTA pair: the injected launch leaves out its
+    first key/value copy, CTA 0's issuer gives up after 1 ms, both CTAs' roles
+    stop on the abort flag or their own limit and meet at the exit barrier; the
+    status word reports the timeout and the next launches are exact."""
+    assert swa.device_status() == 0
+    B, H, Hkv, n, d, w, g = 1, 4, 1, 384, 128, 128, 0
+    x = synthetic.prefill_inputs(B, H, Hkv, n, d, w, g, dtype="bf16", seed=7, device="cuda")
+    swa.inject_stall("prefill", 1_000_000)
+    swa.prefill_cta_pairs(x.Q, x.K, x.V, w, g, x.scale)
+    assert swa.device_status() == -4  # SWA_ERR_DEVICE_TIMEOUT
+    assert swa.device_status() == 0
+    out = swa.prefill_cta_pairs(x.Q, x.K, x.V, w, g, x.scale)
+    ref = swa.prefill(x.Q, x.K, x.V, w, g, x.scale)
+    torch.cuda.synchronize()
+    O, _ = oracle_mod.prefill(x.Q, x.K, x.V, w, g, x.scale)
+    assert_close(out, O, "bf16", "CTA-pair prefill after recovery")
+    assert torch.equal(out, ref)
+    assert swa.device_status() == 0
