@@ -1791,48 +1791,6 @@ int duo_clusters()
     return n;
 }
 
-// The window path on CTA pairs with one head per CTA and double-buffered S
-// and O: see swa_prefill_cl2.cuh.
-#include "swa_prefill_cl2.cuh"
-
-template <int HD>
-int cl2_clusters()
-{
-    static std::atomic<int> known[kMaxDevices];  // 0: not yet known; else clusters + 1
-    const int dev = current_device();
-    if (dev < 0) return 0;
-    const int k = known[dev].load(std::memory_order_acquire);
-    if (k > 0) return k - 1;
-    using L = LayoutC<HD>;
-    int n = 0;
-    if (smem_opt_in<swa_prefill_bf16_cl2_sm103<HD>>(L::DYN_SMEM) == cudaSuccess) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * (num_sms() / 2));
-        cfg.blockDim = dim3(NTHREADS2);
-        cfg.dynamicSmemBytes = L::DYN_SMEM;
-        if (cudaOccupancyMaxActiveClusters(&n, swa_prefill_bf16_cl2_sm103<HD>, &cfg) != cudaSuccess)
-            n = 0;
-    }
-    (void)cudaGetLastError();
-    known[dev].store(n + 1, std::memory_order_release);
-    return n;
-}
-
-// One launch of the one-head-per-CTA pair kernel (window path, even group);
-// SWA_ERR_UNSUPPORTED if no cluster of two fits.
-template <int HD>
-int launch_cl2(const CUtensorMap &mq, const CUtensorMap &mkh, const CUtensorMap &mv,
-               PrefillParams p, cudaStream_t stream)
-{
-    using L = LayoutC<HD>;
-    const int fit = cl2_clusters<HD>();
-    if (fit <= 0) return SWA_ERR_UNSUPPORTED;
-    p.num_items = p.B * (p.H / 2) * p.n_qt;
-    const int clusters = p.num_items < fit ? p.num_items : fit;
-    swa_prefill_bf16_cl2_sm103<HD><<<2 * clusters, NTHREADS2, L::DYN_SMEM, stream>>>(mq, mkh, mv, p);
-    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
-}
-
 // One launch of the CTA-pair kernel (window path, even group, H % 4 == 0);
 // SWA_ERR_UNSUPPORTED if no cluster of two fits.
 template <int HD, bool SHARED>
@@ -1990,10 +1948,12 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     // d = 128, an even group, heads in quads, no narrow sink tile
     if (cta_pairs) {
         if constexpr (HD == 128) {
-            if (!pat && walk == nullptr && p.G % 2 == 0 && !(g >= 1 && g <= NB_SINK)) {
+            if (!pat && walk == nullptr && p.G % 2 == 0 && H % 4 == 0 &&
+                !(g >= 1 && g <= NB_SINK)) {
                 CUtensorMap mkh;
                 if (!make_map_3d(&mkh, K, HD, n_k, ZK, BN / 2)) return SWA_ERR_CUDA;
-                return launch_cl2<HD>(mq, mkh, mv, p, stream);
+                return p.G % 4 == 0 ? launch_duo<HD, true>(mq, mkh, mv, p, stream)
+                                    : launch_duo<HD, false>(mq, mkh, mv, p, stream);
             }
         }
         return SWA_ERR_UNSUPPORTED;

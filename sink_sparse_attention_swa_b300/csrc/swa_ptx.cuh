@@ -580,25 +580,5 @@ __device__ __forceinline__ void mma2_ts_group8(uint32_t d, uint32_t a_tmem, uint
 #undef SWA_MMA2_TS
 }
 
-// Half of mma2_ts_group8: four k-steps (64 keys) from the given P columns and
-// V rows of the CTA's N/2 value columns.
-__device__ __forceinline__ void mma2_ts_group4(uint32_t d, uint32_t a_tmem, uint64_t b,
-                                               uint32_t idesc, uint32_t acc0)
-{
-    const uint32_t bl = static_cast<uint32_t>(b), bh = static_cast<uint32_t>(b >> 32);
-#define SWA_MMA2_TS(AO, BO) \
-    "add.u32 ta, %1, " #AO ";\n\tadd.u32 yl, %2, " #BO ";\n\tmov.b64 yd, {yl, %3};\n\t" \
-    "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], yd, %4, t;\n\t"
-    asm volatile("{\n\t.reg .pred e, f, t;\n\t.reg .b32 ta, yl;\n\t.reg .b64 yd;\n\t"
-                 "elect.sync _|e, 0xffffffff;\n\t"
-                 "setp.ne.b32 f, %5, 0;\n\tsetp.eq.b32 t, %4, %4;\n\t"
-                 "mov.b64 yd, {%2, %3};\n\t"
-                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], yd, %4, f;\n\t"
-                 SWA_MMA2_TS(8, 128) SWA_MMA2_TS(16, 256) SWA_MMA2_TS(24, 384) "}\n" ::"r"(d),
-                 "r"(a_tmem), "r"(bl), "r"(bh), "r"(idesc), "r"(acc0)
-                 : "memory");
-#undef SWA_MMA2_TS
-}
-
 }  // namespace ptx
 }  // namespace swa
