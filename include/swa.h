@@ -65,7 +65,8 @@ typedef enum {
     SWA_ERR_CUDA = -3,           /* a CUDA runtime/driver call failed           */
     SWA_ERR_DEVICE_TIMEOUT = -4, /* a kernel's bounded wait ran out (device)    */
     SWA_ERR_ALLOC = -5,          /* library workspace allocation failed         */
-    SWA_ERR_WORKSPACE = -6       /* caller workspace too small                  */
+    SWA_ERR_WORKSPACE = -6,      /* caller workspace too small                  */
+    SWA_ERR_DEVICE_BOUNDS = -7   /* a debug build's device bounds check failed  */
 } swa_status;
 
 typedef enum { SWA_BF16 = 0, SWA_F32 = 1 } swa_dtype;
@@ -404,6 +405,25 @@ int swa_debug_prefill_cta_pairs(const void *Q, const void *K, const void *V, voi
 #define SWA_STALL_PREFILL 1
 #define SWA_STALL_DECODE 2
 int swa_debug_inject_stall(int kind, int64_t wait_ns);
+
+/*
+ * Debug builds.  The library can be built with SWA_DEBUG defined
+ * (libswa_debug.so beside libswa.so).  Its kernels then check, before each
+ * global store they make and each index they derive from the tile walk, that
+ * the index lies inside its buffer or range (output rows, LSE entries, decode
+ * partials, cache slots, chunk key-list rows, key tiles, work items).  A check
+ * that fails sets a bit in the device status word, so swa_get_device_status()
+ * returns SWA_ERR_DEVICE_BOUNDS, and the store it guards is skipped; nothing
+ * traps.  Product builds compile no checks and never return that status.
+ *
+ * swa_debug_shrink_bounds -- a test aid for debug builds, with no counterpart
+ * on the pages: the next bf16 prefill launch on the current device checks its
+ * output rows against a limit one row short of the real one, so the last
+ * output row of the last head of the last sequence fails its check and is not
+ * written.  Returns SWA_OK in a debug build, SWA_ERR_UNSUPPORTED in a product
+ * build (which has no checks), SWA_ERR_CUDA if no device is current.
+ */
+int swa_debug_shrink_bounds(void);
 
 /* A static string naming a swa_status value. */
 const char *swa_status_string(int status);

@@ -19,6 +19,7 @@ The library is ``libswa.so`` next to this file, built in place by
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -36,9 +37,11 @@ __all__ = [
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.environ.get("SWA_LIBRARY", os.path.join(_PKG, "libswa.so"))
+_LIB_DEBUG_PATH = os.path.join(_PKG, "libswa_debug.so")
 
 STATUS = {0: "SWA_OK", -1: "SWA_ERR_INVALID_ARG", -2: "SWA_ERR_UNSUPPORTED", -3: "SWA_ERR_CUDA",
-          -4: "SWA_ERR_DEVICE_TIMEOUT", -5: "SWA_ERR_ALLOC", -6: "SWA_ERR_WORKSPACE"}
+          -4: "SWA_ERR_DEVICE_TIMEOUT", -5: "SWA_ERR_ALLOC", -6: "SWA_ERR_WORKSPACE",
+          -7: "SWA_ERR_DEVICE_BOUNDS"}
 SWA_BF16, SWA_F32 = 0, 1
 # fixed patterns of swa_prefill_pattern
 PATTERNS = {"window": 0, "dilated": 1, "strided": 2, "landmark": 3}
@@ -69,6 +72,7 @@ SIGNATURES = {
     "swa_debug_inject_stall": (_i, [_i, _i64]),
     "swa_debug_prefill_walk": (_i, [_p] * 4 + [_i] * 5 + [_i] * 4 + [_f, _p, _i64, _p]),
     "swa_debug_prefill_cta_pairs": (_i, [_p, _p, _p, _p, _p] + [_i] * 7 + [_f, _p]),
+    "swa_debug_shrink_bounds": (_i, []),
     "swa_status_string": (ctypes.c_char_p, [_i]),
     "swa_version": (_i, []),
     "swa_selftest_umma": (_i, [_p, _p, _p, _p, _p, _p]),
@@ -84,21 +88,45 @@ class SwaError(RuntimeError):
 _LIB = None
 
 
-def _load():
-    global _LIB
-    if _LIB is not None:
-        return _LIB
-    if not os.path.exists(_LIB_PATH):
+def _bind(path):
+    if not os.path.exists(path):
         raise ImportError(
-            f"libswa.so not found at {_LIB_PATH}; build it with "
+            f"{os.path.basename(path)} not found at {path}; build it with "
             "`python -m sink_sparse_attention_swa_b300.build` (no CPU fallback exists)")
-    lib = ctypes.CDLL(_LIB_PATH)
+    lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _LIB = lib
     return lib
+
+
+def _load():
+    global _LIB
+    if _LIB is None:
+        _LIB = _bind(_LIB_PATH)
+    return _LIB
+
+
+@contextlib.contextmanager
+def debug_build():
+    """Within the block every entry point of this module calls libswa_debug.so
+    (the same kernels with their bounds checks compiled in; see include/swa.h)
+    instead of libswa.so.  Each library keeps its own device status word."""
+    global _LIB
+    prev = _load()
+    _LIB = _bind(_LIB_DEBUG_PATH)
+    try:
+        yield
+    finally:
+        _LIB = prev
+
+
+def shrink_bounds() -> None:
+    """swa_debug_shrink_bounds: in a debug build, the next bf16 prefill checks
+    its output rows against a limit one row short (raises SwaError with
+    SWA_ERR_UNSUPPORTED in a product build)."""
+    _check("swa_debug_shrink_bounds", _load().swa_debug_shrink_bounds())
 
 
 def __getattr__(name):

@@ -430,7 +430,20 @@ int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_sl
     return SWA_OK;
 }
 
-int swa_debug_inject_stall(int kind, int64_t wait_ns) { return set_injected_stall(kind, wait_ns); }
+int swa_debug_inject_stall(int kind, int64_t wait_ns)
+{
+    if (kind != 0 && kind != SWA_STALL_PREFILL && kind != SWA_STALL_DECODE) return SWA_ERR_INVALID_ARG;
+    return set_injected_stall(kind, wait_ns);
+}
+
+int swa_debug_shrink_bounds(void)
+{
+#ifdef SWA_DEBUG
+    return set_injected_stall(INJECT_SHRINK_BOUNDS, 0);
+#else
+    return SWA_ERR_UNSUPPORTED;  // a product build has no checks to shrink
+#endif
+}
 
 int swa_get_device_status(swa_stream_t stream)
 {
@@ -447,6 +460,7 @@ const char *swa_status_string(int status)
     case SWA_ERR_DEVICE_TIMEOUT: return "SWA_ERR_DEVICE_TIMEOUT";
     case SWA_ERR_ALLOC: return "SWA_ERR_ALLOC";
     case SWA_ERR_WORKSPACE: return "SWA_ERR_WORKSPACE";
+    case SWA_ERR_DEVICE_BOUNDS: return "SWA_ERR_DEVICE_BOUNDS";
     default: return "SWA_ERR_UNKNOWN";
     }
 }

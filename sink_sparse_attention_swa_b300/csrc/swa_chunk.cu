@@ -63,8 +63,12 @@ __global__ void swa_chunk_gather_k(T *__restrict__ Kx, T *__restrict__ Vx, const
                     vs = vn + off;
                 }
             }
-            kv = reinterpret_cast<const uint4 *>(ks)[c];
-            vv = reinterpret_cast<const uint4 *>(vs)[c];
+            // debug builds: the row read lies in the cache or the chunk
+            const int pr = W0 + (r - S - pad);
+            if (SWA_BOUNDS(r < S ? r < g : (pr >= 0 && (pr < ps || pr - ps < Tn)), status)) {
+                kv = reinterpret_cast<const uint4 *>(ks)[c];
+                vv = reinterpret_cast<const uint4 *>(vs)[c];
+            }
         }
         reinterpret_cast<uint4 *>(Kx + (bk * rows + r) * HD)[c] = kv;
         reinterpret_cast<uint4 *>(Vx + (bk * rows + r) * HD)[c] = vv;

@@ -307,6 +307,12 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
                 // test injection: this stage's copies never start, so the
                 // consumers' wait for it runs out (nothing is in flight to drain)
                 if (p.skip_first_stage && it == 0) return true;
+                // debug builds: the rows lie in the segment's cache (a copy that
+                // fails the check is not made, and the consumers' wait runs out)
+                if (!SWA_BOUNDS(s.b < p.B && s.kvh < p.Hkv && row >= 0 &&
+                                    static_cast<size_t>(row) + count <= S,
+                                p.status))
+                    return true;
                 const uint32_t bytes = static_cast<uint32_t>(count * C::RB);
                 mbar_expect_tx(FULL(slot), 2 * bytes);
                 const size_t off = ((static_cast<size_t>(s.b) * p.Hkv + s.kvh) * S + row) * HD;
@@ -355,7 +361,8 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
             // a padding head of the sub-group scores with q = 0 (never written out)
-            const bool real = hh < s.nh;
+            const bool real = hh < s.nh &&
+                              SWA_BOUNDS(s.b < p.B && s.h0 + hh < p.H, p.status);
             const T *qr = q + (static_cast<size_t>(s.b) * p.H + s.h0 + (real ? hh : 0)) * HD;
 #pragma unroll
             for (int c = 0; c < C::CPL; ++c) {
@@ -550,7 +557,11 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
         if (!cta_sync(0)) return;
         // the CTA's partial for this segment
         float *wsp = p.ws + (static_cast<size_t>(blockIdx.x) + s.bk) * G * (HD + 2);
-        for (int x = threadIdx.x; x < G * (HD + 2); x += DEC_CWARPS * 32) {
+        // debug builds: the partial's index lies in the workspace (ctas + B*Hv partials)
+        const bool w_ok = SWA_BOUNDS(static_cast<long long>(blockIdx.x) + s.bk <
+                                         static_cast<long long>(p.P) + static_cast<long long>(p.B) * p.Hv,
+                                     p.status);
+        for (int x = threadIdx.x; w_ok && x < G * (HD + 2); x += DEC_CWARPS * 32) {
             const int hh = x / (HD + 2), col = x % (HD + 2);
             float M = M_EMPTY;
 #pragma unroll
@@ -585,7 +596,9 @@ __global__ void __launch_bounds__(G * HD) swa_decode_merge(const DecodeParams p)
     const int bk = blockIdx.x;
     const int hh = threadIdx.x / HD, col = threadIdx.x % HD;
     const long long S = static_cast<long long>(p.w) + p.g;
-    const int c_lo = cta_of(p.T, p.P, bk * S), c_hi = cta_of(p.T, p.P, bk * S + S - 1);
+    int c_lo = cta_of(p.T, p.P, bk * S), c_hi = cta_of(p.T, p.P, bk * S + S - 1);
+    // debug builds: the partials lie in the workspace (else none is read)
+    if (!SWA_BOUNDS(c_lo >= 0 && c_hi < p.P, p.status)) c_hi = c_lo - 1;
     // the first NU partials (usually all of them) are loaded in one round
     constexpr int NU = 4;
     float mv[NU], lv[NU], ov[NU];
@@ -624,6 +637,7 @@ __global__ void __launch_bounds__(G * HD) swa_decode_merge(const DecodeParams p)
     float row_lse;
     const float f = L > 0.f ? finish_row(M, L, p.sink, h, &row_lse) : 0.f;
     if (!(L > 0.f)) row_lse = -INFINITY;
+    if (!SWA_BOUNDS(bh < static_cast<size_t>(p.B) * p.H, p.status)) return;
     static_cast<T *>(p.O)[bh * HD + col] = U::from_f(o * f);
     if (col == 0 && p.lse != nullptr) p.lse[bh] = row_lse;
 }
@@ -693,12 +707,12 @@ __global__ void swa_cache_append_k(T *__restrict__ Kc, T *__restrict__ Vc,
         const uint4 vv = reinterpret_cast<const uint4 *>(vn + row * HD)[c];
         T *kbase = Kc + bk * slots * HD;
         T *vbase = Vc + bk * slots * HD;
-        if (t >= T_new - w) {  // only the last w new positions survive in the ring
+        if (t >= T_new - w && SWA_BOUNDS(p % w < w, status)) {  // the last w survive in the ring
             const size_t slot = static_cast<size_t>(p % w);
             reinterpret_cast<uint4 *>(kbase + slot * HD)[c] = kv;
             reinterpret_cast<uint4 *>(vbase + slot * HD)[c] = vv;
         }
-        if (p < g) {
+        if (p < g && SWA_BOUNDS(static_cast<size_t>(w) + p < slots, status)) {
             const size_t slot = static_cast<size_t>(w) + p;
             reinterpret_cast<uint4 *>(kbase + slot * HD)[c] = kv;
             reinterpret_cast<uint4 *>(vbase + slot * HD)[c] = vv;

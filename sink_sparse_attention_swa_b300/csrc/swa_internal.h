@@ -188,7 +188,20 @@ __device__ __forceinline__ float finish_row(float m, float l, const float *sink,
 // Device status word (one per device, in swa_status.cu).  Kernels OR an error
 // code into it when a bounded wait runs out.
 // ---------------------------------------------------------------------------
-enum : int { DEV_ERR_TIMEOUT = 1, DEV_ERR_BAD_POS = 2 };
+enum : int { DEV_ERR_TIMEOUT = 1, DEV_ERR_BAD_POS = 2, DEV_ERR_BOUNDS = 4 };
+
+// Bounds checks of the debug build (compiled with SWA_DEBUG): SWA_BOUNDS(cond,
+// status) is cond, and when cond is false it also records DEV_ERR_BOUNDS in
+// the device status word; the caller skips the access it guards.  In the
+// product build it is the constant true and its arguments are not compiled.
+#ifdef SWA_DEBUG
+#define SWA_BOUNDS(cond, status) ((cond) || (atomicOr((status), DEV_ERR_BOUNDS), false))
+#else
+#define SWA_BOUNDS(cond, status) true
+#endif
+// the injection of swa_debug_shrink_bounds (an internal kind of the one-shot
+// launch settings below)
+constexpr int INJECT_SHRINK_BOUNDS = 3;
 
 int *status_ptr();          // device address of the current device's status word
 int read_and_clear_status(cudaStream_t stream);

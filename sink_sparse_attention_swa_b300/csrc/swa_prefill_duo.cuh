@@ -493,8 +493,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS2, 1)
                 const float2 sv = stats[((it & 1) * 2 + x) * BM + r];
                 const int h = 4 * q + 2 * x + rank;
                 const int t_row = tr.q0 + r - off;
-                const bool row_ok = t_row < p.n;
                 const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n + t_row;
+                const bool row_ok =
+                    t_row < p.n && SWA_BOUNDS(static_cast<long long>(orow_i) < p.dbg_orows, p.status);
                 store_o_rows_chunked<HD, true>(tmem + lane_off + x * 256, sv.x, p.O + orow_i * HD,
                                                row_ok, stage, lane, LBAR(L::O_EMPTY + x));
                 if (p.lse != nullptr && row_ok) p.lse[orow_i] = sv.y;

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(TM)
                          const float *__restrict__ V, float *__restrict__ O,
                          float *__restrict__ lse, const float *__restrict__ sink, int H,
                          int Hkv, int n, int n_k, int w, int g, float sl2,
-                         const int32_t *__restrict__ pos0, int R, int rl)
+                         const int32_t *__restrict__ pos0, int R, int rl, int *status)
 {
     __shared__ __align__(16) float sK[TN][HD];
     __shared__ __align__(16) float sV[TN][HD];
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(TM)
         }
         m = m_new;
     }
-    if (t < nq) {
+    if (t < nq && SWA_BOUNDS(qrow < static_cast<size_t>(gridDim.z) * H * n, status)) {
         float row_lse;
         const float inv = finish_row(m, l, sink, h, &row_lse);
 #pragma unroll
@@ -130,7 +130,7 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     swa_prefill_f32_simt<HD><<<grid, TM, 0, stream>>>(
         static_cast<const float *>(Q), static_cast<const float *>(K),
         static_cast<const float *>(V), static_cast<float *>(O), lse, sink, H, Hkv, n, n_k, w, g,
-        scale * 1.4426950408889634f, pos0, R, rl);
+        scale * 1.4426950408889634f, pos0, R, rl, status_ptr());
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 

@@ -113,6 +113,9 @@ struct PrefillParams {
     int *status;
     uint64_t wait_ns;   // limit of every bounded wait of the roles (2 s unless a test sets it)
     int skip_first_kv;  // test injection: the first key/value copy is left out (see swa.h)
+#ifdef SWA_DEBUG
+    long long dbg_orows;  // output rows the bounds checks allow (B*H*n; one fewer when shrunk)
+#endif
 };
 
 // One entry of the tile-walk log per key tile a producer issues: the item's
@@ -232,6 +235,19 @@ __device__ __forceinline__ KeyTile key_tile(const TileRange &tr, int j, const Pr
     }
     return kt;
 }
+
+// Debug builds: the key tile's first key lies in the key list it is read
+// from (the keys, the landmark list, or the residue class's subsequence).
+template <bool PAT>
+__device__ __forceinline__ bool key_tile_in_range(const KeyTile &kt, int cls, const PrefillParams &p)
+{
+    if constexpr (!PAT) return kt.k0 >= 0 && kt.k0 < p.n_k;
+    const int lim = kt.land ? (p.n_k + p.rl - 1) / p.rl : (cls < p.rem ? p.n_hi : p.n_lo);
+    return kt.k0 >= 0 && kt.k0 < lim;
+}
+#define SWA_ITEM_IN_RANGE(p, b, kvh, qt, cls) \
+    ((b) >= 0 && (b) < (p).B && (kvh) >= 0 && (kvh) < (p).Hkv && (qt) >= 0 && (qt) < (p).n_qt && \
+     (cls) >= 0 && (cls) < (p).R)
 
 __device__ __forceinline__ float ex2(float x)
 {
@@ -471,6 +487,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int t = blockIdx.x; ok && t < p.num_items; t += gridDim.x, ++it) {
                 int b, hg, kvh, qt, cls;
                 decode_level_item<PAT>(t, p, p.G, b, hg, kvh, qt, cls);
+                (void)SWA_BOUNDS(SWA_ITEM_IN_RANGE(p, b, kvh, qt, cls), p.status);
                 int off;
                 const TileRange tr = item_tiles<PAT>(p, b, qt, cls, off);
                 for (int j = 0; j < tr.count; ++j, ++kv_iter) {
@@ -482,6 +499,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         break;
                     }
                     const KeyTile kt = key_tile<PAT>(tr, j, p);
+                    (void)SWA_BOUNDS(key_tile_in_range<PAT>(kt, cls, p), p.status);
                     const int zkv = b * p.Hkv + kvh;
                     // landmark tiles: class 0 of the stride-rl view; others: this class
                     const int kc = kt.land ? 0 : cls;
@@ -763,9 +781,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // the query row of this thread: its index in the class subsequence,
             // and its position c + R t
             const int t_row = i - off;
-            const bool row_ok = t_row < (!PAT ? p.n : cls < p.rem ? p.n_hi : p.n_lo);
             const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n +
                                   (PAT ? cls + static_cast<size_t>(p.R) * t_row : t_row);
+            const bool row_ok = t_row < (!PAT ? p.n : cls < p.rem ? p.n_hi : p.n_lo) &&
+                                SWA_BOUNDS(static_cast<long long>(orow_i) < p.dbg_orows, p.status);
             __nv_bfloat16 *orow = p.O + orow_i * HD;
             store_o_rows<HD>(tmem + lane_off, inv_l, orow, row_ok,
                              smem + L::STAGE_OFF + (warp - 2) * STAGE_WARP, lane);
@@ -1033,6 +1052,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                      t = pair_item_rank(blockIdx.x, ++it)) {
                     int b, hp, kvh, qt, cls;
                     decode_level_item<PAT>(t, p, pair_units<QP>(p), b, hp, kvh, qt, cls);
+                    (void)SWA_BOUNDS(SWA_ITEM_IN_RANGE(p, b, kvh, qt, cls), p.status);
                     int off;
                     const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
                     item_info[it & 3] = tr.count;
@@ -1060,6 +1080,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                             break;
                         }
                         const KeyTile kt = key_tile<PAT>(tr, j, p);
+                        (void)SWA_BOUNDS(key_tile_in_range<PAT>(kt, cls, p), p.status);
                         const int zkv = b * p.Hkv + kvh;
                         // landmark tiles: class 0 of the stride-rl view; others: this class
                         const int kc = kt.land ? 0 : cls;
@@ -1120,6 +1141,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                      t = pair_item_rank(blockIdx.x, ++it)) {
                     int b, hp, kvh, qt, cls;
                     decode_level_item<PAT>(t, p, pair_units<QP>(p), b, hp, kvh, qt, cls);
+                    (void)SWA_BOUNDS(SWA_ITEM_IN_RANGE(p, b, kvh, qt, cls), p.status);
                     int off;
                     const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
                     const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
@@ -1157,6 +1179,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                             break;
                         }
                         const KeyTile kt = key_tile<PAT>(tr, j, p);
+                        (void)SWA_BOUNDS(key_tile_in_range<PAT>(kt, cls, p), p.status);
                         const int zkv = b * p.Hkv + kvh;
                         // landmark tiles: class 0 of the stride-rl view; others: this class
                         const int kc = kt.land ? 0 : cls;
@@ -1590,9 +1613,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 // this thread's query row: half x of a q-tile pair is q tile 2k + x
                 const int i = tr.q0 + (QP ? x * BM : 0) + r;
                 const int t_row = i - off;
-                const bool row_ok = t_row < nq;
                 const size_t orow_i = static_cast<size_t>(b * p.H + h) * p.n +
                                       (PAT ? cls + static_cast<size_t>(p.R) * t_row : t_row);
+                const bool row_ok =
+                    t_row < nq && SWA_BOUNDS(static_cast<long long>(orow_i) < p.dbg_orows, p.status);
                 store_o_rows_chunked<HD>(tmem + lane_off + x * 256, sv.x, p.O + orow_i * HD,
                                          row_ok, stage, lane, BAR(L::O_EMPTY + x));
                 if (p.lse != nullptr && row_ok) p.lse[orow_i] = sv.y;
@@ -1941,6 +1965,13 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     if (p.status == nullptr) return SWA_ERR_CUDA;
     p.wait_ns = TIMEOUT_NS;
     p.skip_first_kv = take_injected_stall(SWA_STALL_PREFILL, &p.wait_ns) ? 1 : 0;
+#ifdef SWA_DEBUG
+    {
+        uint64_t unused = 0;
+        p.dbg_orows = static_cast<long long>(B) * H * n -
+                      (take_injected_stall(INJECT_SHRINK_BOUNDS, &unused) ? 1 : 0);
+    }
+#endif
     // the logged walk is a kernel of its own, so the product kernels carry no
     // per-tile check for it
     // the window path on CTA pairs, on request only (it measured 4-9% slower

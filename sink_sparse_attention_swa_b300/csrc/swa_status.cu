@@ -7,7 +7,8 @@
 namespace swa {
 
 // Bit 0: a bounded wait ran out (DEV_ERR_TIMEOUT); bit 1: a negative
-// position was passed to decode or append (DEV_ERR_BAD_POS).
+// position was passed to decode or append (DEV_ERR_BAD_POS); bit 2: a debug
+// build's bounds check failed (DEV_ERR_BOUNDS).
 __device__ int g_swa_device_status;
 
 namespace {
@@ -33,8 +34,12 @@ bool take_injected_stall(int kind, uint64_t *wait_ns)
 
 int set_injected_stall(int kind, int64_t wait_ns)
 {
-    if (kind != 0 && kind != SWA_STALL_PREFILL && kind != SWA_STALL_DECODE) return SWA_ERR_INVALID_ARG;
-    if (kind != 0 && (wait_ns < 100000 || wait_ns > 2000000000)) return SWA_ERR_INVALID_ARG;
+    if (kind != 0 && kind != SWA_STALL_PREFILL && kind != SWA_STALL_DECODE &&
+        kind != INJECT_SHRINK_BOUNDS)
+        return SWA_ERR_INVALID_ARG;
+    if ((kind == SWA_STALL_PREFILL || kind == SWA_STALL_DECODE) &&
+        (wait_ns < 100000 || wait_ns > 2000000000))
+        return SWA_ERR_INVALID_ARG;
     const int dev = current_device();
     if (dev < 0) return SWA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -87,6 +92,7 @@ int read_and_clear_status(cudaStream_t stream)
     const int zero = 0;
     if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SWA_ERR_CUDA;
     if (v & DEV_ERR_TIMEOUT) return SWA_ERR_DEVICE_TIMEOUT;
+    if (v & DEV_ERR_BOUNDS) return SWA_ERR_DEVICE_BOUNDS;
     if (v & DEV_ERR_BAD_POS) return SWA_ERR_INVALID_ARG;
     return SWA_OK;
 }

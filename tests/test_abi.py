@@ -31,6 +31,18 @@ def test_library_exports_every_declared_symbol(swa):
     assert set(declared_functions()) == set(swa.SIGNATURES)
 
 
+def test_debug_library_exports_every_declared_symbol(swa):
+    """libswa_debug.so (the kernels with their bounds checks) offers the same
+    boundary; the product build has no checks to shrink."""
+    lib = ctypes.CDLL(swa._LIB_DEBUG_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert swa.lib.swa_debug_shrink_bounds() == -2  # SWA_ERR_UNSUPPORTED
+    with swa.debug_build():
+        assert swa.lib.swa_version() >= 100
+        assert swa.lib.swa_status_string(-7).decode() == "SWA_ERR_DEVICE_BOUNDS"
+
+
 def test_version_and_status_strings(swa):
     assert swa.lib.swa_version() >= 100
     for code, name in swa.STATUS.items():
