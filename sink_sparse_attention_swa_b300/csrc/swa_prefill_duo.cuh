@@ -153,6 +153,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS2, 1)
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+#ifdef SWA_DEBUG
+    if (!tmem_base_ok(tmem, p.status)) goto teardown;
+#endif
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
@@ -506,6 +509,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS2, 1)
 #undef BAR
     // neither CTA leaves (nor frees its tensor memory) while the other may
     // still reach its barriers or tensor memory
+#ifdef SWA_DEBUG
+teardown:
+#endif
     tc_fence_before();
     cluster_sync();
     tc_fence_after();

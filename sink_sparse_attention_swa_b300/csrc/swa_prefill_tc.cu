@@ -59,6 +59,23 @@ constexpr uint32_t S_COL0 = 128;
 constexpr uint32_t P_COL0 = 384;
 constexpr float RESCALE_LOG2 = 8.0f;
 
+// Tensor-memory columns are compile-time offsets from the allocated base.
+// One-head kernel: O in [0, HD), two S buffers from S_COL0, two P halves from
+// P_COL0.  Head-pair kernels: O_X at 256x, S_X / P_X at 256x + 128.
+static_assert(S_COL0 >= 128 && P_COL0 >= S_COL0 + 2 * BN && P_COL0 + 2 * (BN / 2) <= TMEM_COLS,
+              "one-head kernel's tensor-memory columns");
+static_assert(256 + 128 + BN <= TMEM_COLS, "head-pair kernels' tensor-memory columns");
+
+#ifdef SWA_DEBUG
+// Debug builds: the base the allocator returned is lane 0, with every
+// allocated column after it inside the SM's 512.  A kernel whose base fails
+// skips its work and goes straight to its teardown.
+__device__ __forceinline__ bool tmem_base_ok(uint32_t tmem, int *status)
+{
+    return SWA_BOUNDS((tmem >> 16) == 0u && (tmem & 0xFFFFu) + TMEM_COLS <= 512u, status);
+}
+#endif
+
 // Epilogue staging: each softmax warp turns its 32 rows x 32 columns of the
 // output (64 bytes of bf16 per row) around in shared memory so that its global
 // stores cover whole 64-byte row segments, 8 rows per instruction, instead of
@@ -458,6 +475,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+#ifdef SWA_DEBUG
+    if (!tmem_base_ok(tmem, p.status)) goto teardown;
+#endif
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -795,6 +815,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
 #undef BAR
+#ifdef SWA_DEBUG
+teardown:
+#endif
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1034,6 +1057,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+#ifdef SWA_DEBUG
+    if (!tmem_base_ok(tmem, p.status)) goto teardown;
+#endif
 
     if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
@@ -1624,6 +1650,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         }
     }
 #undef BAR
+#ifdef SWA_DEBUG
+teardown:
+#endif
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
