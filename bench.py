@@ -678,8 +678,9 @@ def decode_leg(args, swa, synthetic, world, rank, local, dev, stream, flush, pk)
                                        sink_scale=dc["sink_scale"], device=dev)
     kn, vn = synthetic.token_stream(dc["B"], dc["Hkv"], dc["d"], 1, seed=rank + 1, device=dev)
     dout = torch.empty_like(dx.q)
-    splits = 0
-    ws_bytes = swa.decode_workspace_bytes(dc["B"], dc["H"], dc["Hkv"], dc["d"], dc["w"], dc["g"])
+    splits = args.splits  # 0: the library's automatic, balanced split
+    ws_bytes = swa.decode_workspace_bytes(dc["B"], dc["H"], dc["Hkv"], dc["d"], dc["w"], dc["g"],
+                                          splits)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     dfn_dec = lambda: swa.decode(dx.q, dx.Kc, dx.Vc, dx.pos, dc["w"], dc["g"], dx.scale, out=dout,
                                  workspace=ws, num_splits=splits, stream=stream)
@@ -700,7 +701,7 @@ def decode_leg(args, swa, synthetic, world, rank, local, dev, stream, flush, pk)
     assert swa.device_status(stream) == 0, "device status reported an error"
     return {"workload": "streaming_decode_sinks", **{k: dc[k] for k in dc},
             "value": dgbs, "unit": "GB/s", "ms_per_step": dms,
-            "step": "cache append (1 token) + decode",
+            "step": "cache append (1 token) + decode", "num_splits": splits or "auto",
             "roofline": {"bound": "hbm", "achieved": dbytes / (dec_ms * 1e-3) / 1e9,
                          "peak": pk["hbm"], "unit": "GB/s",
                          "frac": dbytes / (dec_ms * 1e-3) / 1e9 / pk["hbm"],
@@ -765,6 +766,8 @@ def main():
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other configurations (Gemma-3-like, long-context, tiny fp32)")
     ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "chunk"])
+    ap.add_argument("--splits", type=int, default=0,
+                    help="decode split count for tuning sweeps (0: automatic)")
     ap.add_argument("--workload", default="mistral_like_prefill", choices=sorted(PREFILL_WORKLOADS))
     args = ap.parse_args()
     if args.warmup < 3:
