@@ -26,6 +26,9 @@
  *  - d is 64 or 128.  Element type bf16 (accumulation in fp32) or fp32.
  *  - All tensor pointers are device pointers owned by the caller, 16-byte
  *    aligned.  The library never frees caller memory.
+ *  - Kernels launch on the calling thread's current CUDA device
+ *    (cudaGetDevice); every pointer of a call and its stream must belong to
+ *    that device.
  *  - Every launch is asynchronous on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream).  SWA_OK means "validated and enqueued".  A
  *    device-side wait that runs out of time marks the library's device status
@@ -327,13 +330,15 @@ int swa_enumerate_landmark_tiles(int64_t n, int64_t w, int64_t g, int64_t r, int
  * at index t + *query_offset.  The prefill kernels read index j for query
  * index i when j <= i and (j >= i-w+1 or j < g).  `position` is host memory of
  * `cap` int64 elements.  Returns the number of rows written (the workspace
- * rows of swa_prefill_chunk_workspace_bytes), or SWA_ERR_INVALID_ARG.
+ * rows of swa_prefill_chunk_workspace_bytes), or SWA_ERR_INVALID_ARG (also
+ * when the list would exceed `cap` or INT32_MAX rows; nothing is written then).
  */
 int swa_chunk_key_positions(int64_t pos0, int w, int g, int T, int64_t *position, size_t cap,
                             int32_t *query_offset);
 
 /* Where the rolling cache keeps position p: *ring_slot = p mod w,
- * *sink_slot = w+p if p < g else -1.  Returns SWA_OK or SWA_ERR_INVALID_ARG. */
+ * *sink_slot = w+p if p < g else -1.  Returns SWA_OK, or SWA_ERR_INVALID_ARG
+ * if p < 0, w < 1, g < 0, w + g > INT32_MAX or an output pointer is null. */
 int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_slot);
 
 /* ---------------------------------------------------------------------- */

@@ -4,8 +4,9 @@ A thin ctypes binding over ``libswa.so`` (C ABI in ``include/swa.h``).  The
 functions here only marshal arguments -- shapes, dtypes, pointers, the stream
 -- and call the library; every step of the computation runs in the library's
 CUDA kernels.  Tensors are torch CUDA tensors (torch is used for device memory
-and streams only).  The library is loaded on first use; if it is missing that
-first call raises ImportError: there is no fallback.
+and streams only), all on one device, which each call makes current while it
+runs.  The library is loaded on first use; if it is missing that first call
+raises ImportError: there is no fallback.
 
     prefill(q, k, v, w, g=0, scale=None, out=None, lse=None)        -> out
     prefill_pattern(q, k, v, pattern, w, g=0, r=1, ...)             -> out
@@ -21,6 +22,7 @@ from __future__ import annotations
 
 import contextlib
 import ctypes
+import functools
 import math
 import os
 
@@ -147,6 +149,8 @@ def _check(name: str, rc: int) -> None:
 def _stream(stream, device) -> int:
     if stream is None:
         stream = torch.cuda.current_stream(device)
+    elif isinstance(stream, torch.cuda.Stream) and device is not None and stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -154,9 +158,26 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _on_device(fn):
+    """Runs an entry point with the device of its first tensor argument as the
+    current CUDA device: the library launches on the current device, and every
+    tensor of the call must live there (checked by _need)."""
+    @functools.wraps(fn)
+    def call(*args, **kwargs):
+        t = args[0] if args else None
+        if isinstance(t, torch.Tensor) and t.is_cuda:
+            with torch.cuda.device(t.device):
+                return fn(*args, **kwargs)
+        return fn(*args, **kwargs)
+    return call
+
+
 def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, not on cuda:{torch.cuda.current_device()} "
+                         "with the call's other tensors")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -165,6 +186,7 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+@_on_device
 def prefill(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None, lse=None,
             stream=None, sink_logit=None):
     """q [B,H,n,d], k/v [B,Hkv,n,d] (bf16 or fp32, CUDA) -> out [B,H,n,d].
@@ -197,6 +219,7 @@ def prefill(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None, l
     return out
 
 
+@_on_device
 def prefill_pattern(q, k, v, pattern: str, w: int = 1, g: int = 0, r: int = 1,
                     scale: float | None = None, out=None, lse=None, sink_logit=None, stream=None):
     """Prefill under a fixed pattern (swa_prefill_pattern): "window" (w, g),
@@ -227,6 +250,7 @@ def prefill_pattern(q, k, v, pattern: str, w: int = 1, g: int = 0, r: int = 1,
     return out
 
 
+@_on_device
 def prefill_chunk(q, k_new, v_new, k_cache, v_cache, pos0, w: int, g: int = 0,
                   scale: float | None = None, out=None, lse=None, sink_logit=None,
                   append: bool = False, workspace=None, stream=None):
@@ -257,6 +281,7 @@ def prefill_chunk(q, k_new, v_new, k_cache, v_cache, pos0, w: int, g: int = 0,
                                                            _DT[q.dtype]))
     if workspace is None:
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace")
     ws_bytes = workspace.numel() * workspace.element_size()
     rc = _load().swa_prefill_chunk(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                    _ptr(v_cache), _ptr(pos0), _ptr(out), _ptr(lse),
@@ -276,6 +301,7 @@ def decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits=0) -> int:
     return int(_load().swa_decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits))
 
 
+@_on_device
 def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = None, out=None,
            lse=None, num_splits: int = 0, workspace=None, stream=None, sink_logit=None):
     """q [B,H,d]; k_cache/v_cache [B,Hkv,w+g,d]; pos int32 [B] (CUDA) -> out [B,H,d].
@@ -303,6 +329,8 @@ def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = N
     nbytes = decode_workspace_bytes(B, H, Hkv, d, w, g, num_splits)
     if workspace is None and nbytes > 0:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if workspace is not None:
+        _need(workspace, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if sink_logit is not None:
         _need(sink_logit, "sink_logit", torch.float32, (H,))
@@ -319,6 +347,7 @@ def decode(q, k_cache, v_cache, pos, w: int, g: int = 0, scale: float | None = N
     return out
 
 
+@_on_device
 def cache_append(k_cache, v_cache, k_new, v_new, pos0, w: int, g: int = 0, stream=None):
     """Write k_new/v_new [B,Hkv,T,d] at positions pos0[b] .. pos0[b]+T-1 into the
     rolling caches [B,Hkv,w+g,d] (ring slot p mod w; sink slot w+p for p < g)."""
@@ -384,6 +413,7 @@ def device_status(stream=None) -> int:
 WALK_FIELDS = ("item", "b", "kvh", "unit", "qtile", "cls", "k0", "flags")
 
 
+@_on_device
 def prefill_cta_pairs(q, k, v, w: int, g: int = 0, scale: float | None = None, out=None,
                       lse=None, stream=None):
     """The bf16 window-path prefill on the CTA-pair kernel
@@ -408,6 +438,7 @@ def prefill_cta_pairs(q, k, v, w: int, g: int = 0, scale: float | None = None, o
     return out
 
 
+@_on_device
 def prefill_walk(q, k, v, pattern: str, w: int, g: int = 0, r: int = 1,
                  scale: float | None = None, max_entries: int = 1 << 20, stream=None):
     """Diagnostic (swa_debug_prefill_walk): runs the bf16 prefill and returns
@@ -444,6 +475,7 @@ def inject_stall(kind: str, wait_ns: int = 1_000_000) -> None:
     _check("swa_debug_inject_stall", _load().swa_debug_inject_stall(STALL_KINDS[kind], int(wait_ns)))
 
 
+@_on_device
 def selftest_umma(A, Bk, Bn, stream=None):
     """Diagnostic: (A @ Bk^T, A @ Bn) computed by the tensor-core operand paths
     the prefill kernel uses; A/Bk/Bn [128,128] bf16 CUDA."""

@@ -403,7 +403,8 @@ int swa_chunk_key_positions(int64_t pos0, int w, int g, int T, int64_t *position
         static_cast<long long>(w) + g > INT32_MAX)
         return SWA_ERR_INVALID_ARG;
     const long long rows = chunk_rows_max(w, g, T);
-    if (static_cast<unsigned long long>(rows) > cap) return SWA_ERR_INVALID_ARG;
+    // the row count is the return value, so it must stay below the error codes' range
+    if (rows > INT32_MAX || static_cast<unsigned long long>(rows) > cap) return SWA_ERR_INVALID_ARG;
     const int ps = static_cast<int>(pos0);
     const int S = chunk_sinks(ps, g), W0 = chunk_w0(ps, w, g), pad = chunk_pad(ps, w, g);
     const long long L = static_cast<long long>(chunk_keys(ps, w, g, T));
@@ -423,7 +424,8 @@ int swa_chunk_key_positions(int64_t pos0, int w, int g, int T, int64_t *position
 
 int swa_cache_slot(int64_t p, int w, int g, int32_t *ring_slot, int32_t *sink_slot)
 {
-    if (p < 0 || w < 1 || g < 0 || ring_slot == nullptr || sink_slot == nullptr)
+    if (p < 0 || w < 1 || g < 0 || static_cast<long long>(w) + g > INT32_MAX ||
+        ring_slot == nullptr || sink_slot == nullptr)
         return SWA_ERR_INVALID_ARG;
     *ring_slot = static_cast<int32_t>(p % w);
     *sink_slot = (p < g) ? static_cast<int32_t>(w + p) : -1;

@@ -87,6 +87,19 @@ def test_cache_slot_matches_oracle(swa, oracle_mod):
             assert swa.cache_slot(p, w, g) == oracle_mod.cache_slots(p, w, g), (p, w, g)
     with pytest.raises(swa.SwaError):
         swa.cache_slot(-1, 3, 0)
+    with pytest.raises(swa.SwaError):  # w + g past INT32_MAX: the sink slot w + p would wrap
+        swa.cache_slot(5, 2**31 - 10, 20)
+
+
+def test_chunk_key_positions_refuses_lists_past_int32(swa):
+    """The row count is the return value: a list of more than INT32_MAX rows is
+    refused before anything is written (the buffer here holds one row)."""
+    import ctypes
+    one = ctypes.c_int64(7)
+    off = ctypes.c_int32(0)
+    rc = swa.lib.swa_chunk_key_positions(0, 2**31 - 200, 0, 2**30, ctypes.addressof(one), 2**62,
+                                         ctypes.byref(off))
+    assert rc == -1 and one.value == 7
 
 
 FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced

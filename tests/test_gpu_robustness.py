@@ -239,3 +239,26 @@ def test_second_device_after_the_first(swa, oracle_mod):
             O2, _ = oracle_mod.decode_cache(c.q, c.Kc, c.Vc, c.pos.cpu().numpy(), 64, 4, c.scale)
             assert_close(o2, O2, "bf16", f"decode on device {dev}")
             assert swa.device_status() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.skipif(not torch.cuda.is_available() or torch.cuda.device_count() < 2,
+                    reason="needs two GPUs")
+def test_binding_runs_on_the_tensors_device(swa, oracle_mod):
+    """The library launches on the current device; the binding makes the device
+    of a call's tensors current for the call, and refuses tensors or a stream
+    on another device before anything is launched."""
+    with torch.cuda.device(0):
+        x = synthetic.prefill_inputs(1, 4, 2, 300, 128, 64, 4, dtype="bf16", seed=5,
+                                     device="cuda:1")
+        out = swa.prefill(x.Q, x.K, x.V, 64, 4, x.scale)
+        assert out.device == torch.device("cuda:1")
+        torch.cuda.synchronize(1)
+        O, _ = oracle_mod.prefill(x.Q, x.K, x.V, 64, 4, x.scale)
+        assert_close(out, O, "bf16", "prefill with its tensors on device 1")
+        with pytest.raises(ValueError):
+            swa.prefill(x.Q, x.K.to("cuda:0"), x.V, 64, 4, x.scale)
+        with pytest.raises(ValueError):
+            swa.prefill(x.Q, x.K, x.V, 64, 4, x.scale, stream=torch.cuda.Stream(device=0))
+    with torch.cuda.device(1):
+        assert swa.device_status() == 0
