@@ -36,10 +36,13 @@
 //   * and accumulates P.V with 16 lanes per value row.
 // When its range leaves a segment, the CTA merges its warps and writes one
 // partial (m, l, o) per head for that segment.
-// Merge pass (swa_decode_merge): per (sequence, kv head), the log-sum-exp
-// merge of the partials of the CTAs whose ranges met the segment.  It is
-// launched as a programmatic dependent launch, so its launch overlaps the
-// split pass; it waits for the split pass to complete before reading.
+// Merge pass (swa_decode_merge): per (sequence, kv head) and head of the
+// group, the log-sum-exp merge of the partials of the CTAs whose ranges met
+// the segment.  It is launched as a programmatic dependent launch, so its
+// launch overlaps the split pass; it waits for the split pass to complete
+// before reading.  Its blocks are small (one head, HD threads, at most 64
+// registers each), so one fits on each SM beside the two split CTAs and is
+// already resident when the split pass ends.
 #include <cmath>
 #include <cstdlib>
 
@@ -587,14 +590,15 @@ __global__ void __launch_bounds__(DEC_THREADS, DecCfg<T, HD, G>::MIN_BLOCKS)
 #undef SYNC
 }
 
+// Block (segment bk, head hh of the sub-group); thread col is one output column.
 template <typename T, int HD, int G>
-__global__ void __launch_bounds__(G * HD) swa_decode_merge(const DecodeParams p)
+__global__ void __launch_bounds__(HD, 8) swa_decode_merge(const DecodeParams p)
 {
     using U = Unpack<T>;
     // wait until the split pass has completed and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int bk = blockIdx.x;
-    const int hh = threadIdx.x / HD, col = threadIdx.x % HD;
+    const int hh = blockIdx.y, col = threadIdx.x;
     const long long S = static_cast<long long>(p.w) + p.g;
     int c_lo = cta_of(p.T, p.P, bk * S), c_hi = cta_of(p.T, p.P, bk * S + S - 1);
     // debug builds: the partials lie in the workspace (else none is read)
@@ -652,8 +656,8 @@ int launch_decode_t(const void *q, const void *Kc, const void *Vc, const DecodeP
         static_cast<const T *>(q), static_cast<const T *>(Kc), static_cast<const T *>(Vc), p);
     if (cudaGetLastError() != cudaSuccess) return SWA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.Hv));
-    cfg.blockDim = dim3(G * HD);
+    cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.Hv), static_cast<unsigned>(G));
+    cfg.blockDim = dim3(HD);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
