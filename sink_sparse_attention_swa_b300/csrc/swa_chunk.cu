@@ -64,7 +64,7 @@ __global__ void swa_chunk_gather_k(T *__restrict__ Kx, T *__restrict__ Vx, const
                 }
             }
             // debug builds: the row read lies in the cache or the chunk
-            const int pr = W0 + (r - S - pad);
+            [[maybe_unused]] const int pr = W0 + (r - S - pad);
             if (SWA_BOUNDS(r < S ? r < g : (pr >= 0 && (pr < ps || pr - ps < Tn)), status)) {
                 kv = reinterpret_cast<const uint4 *>(ks)[c];
                 vv = reinterpret_cast<const uint4 *>(vs)[c];
