@@ -368,8 +368,8 @@ int swa_get_device_status(swa_stream_t stream);
  * kvh*G + u (odd groups under the other patterns); q tiles and key indices
  * count 128-row tiles and rows of the residue class's subsequence for the
  * dilated and strided patterns, and landmark-list entries for landmark tiles.
- * flags: 1 the tile needs no element mask, 2 a landmark tile, 4 the narrow sink
- * tile (16 keys).  Returns as swa_prefill_pattern.
+ * flags: 1 the tile needs no element mask, 2 a landmark tile.  Returns as
+ * swa_prefill_pattern.
  */
 int swa_debug_prefill_walk(const void *Q, const void *K, const void *V, void *O, int B, int H,
                            int Hkv, int n, int d, swa_pattern pattern, int w, int g, int r,
@@ -384,8 +384,7 @@ int swa_debug_prefill_walk(const void *Q, const void *K, const void *V, void *O,
  * swa_prefill_ex; it measured slower than the default kernel on this build's
  * workloads and is kept as a tested alternative, not used by the other entry
  * points.  Arguments, layouts and errors as swa_prefill_ex (dtype bf16), plus
- * SWA_ERR_UNSUPPORTED unless d == 128, H / Hkv is even, H % 4 == 0 and g is 0
- * or above 16.
+ * SWA_ERR_UNSUPPORTED unless d == 128, H / Hkv is even and H % 4 == 0.
  */
 int swa_debug_prefill_cta_pairs(const void *Q, const void *K, const void *V, void *O, float *lse,
                                 int B, int H, int Hkv, int n, int d, int w, int g, float scale,

@@ -418,8 +418,8 @@ def prefill_cta_pairs(q, k, v, w: int, g: int = 0, scale: float | None = None, o
                       lse=None, stream=None):
     """The bf16 window-path prefill on the CTA-pair kernel
     (swa_debug_prefill_cta_pairs): same arguments and result as prefill();
-    raises SwaError (SWA_ERR_UNSUPPORTED) unless d == 128, H / Hkv is even,
-    H % 4 == 0 and g is 0 or above 16."""
+    raises SwaError (SWA_ERR_UNSUPPORTED) unless d == 128, H / Hkv is even and
+    H % 4 == 0."""
     _need(q, "q", torch.bfloat16)
     B, H, n, d = q.shape
     Hkv = k.shape[1]

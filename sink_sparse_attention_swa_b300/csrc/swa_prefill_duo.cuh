@@ -387,29 +387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS2, 1)
                 const KeyTile kt = key_tile<false>(tr, j, p);
                 if (!kt.full) {
                     // k <= i and (k >= i-w+1 or k < g), in tile columns
-                    const int ca = lo - kt.k0, cb = i - kt.k0, cg = p.g - kt.k0;
-                    if (cg >= ca || ca <= 0) {
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (qq * 32 + e > cb) s[qq][e] = __float_as_uint(-INFINITY);
-                    } else if (cb >= BN - 1 && cg <= 0) {
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (qq * 32 + e < ca) s[qq][e] = __float_as_uint(-INFINITY);
-                    } else {
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                const int cc = qq * 32 + e;
-                                if (!(cc <= cb && (cc >= ca || cc < cg)))
-                                    s[qq][e] = __float_as_uint(-INFINITY);
-                            }
-                    }
+                    mask_cols(s, lo - kt.k0, i - kt.k0, p.g - kt.k0);
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll

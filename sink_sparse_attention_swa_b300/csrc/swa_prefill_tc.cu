@@ -59,6 +59,71 @@ constexpr uint32_t S_COL0 = 128;
 constexpr uint32_t P_COL0 = 384;
 constexpr float RESCALE_LOG2 = 8.0f;
 
+// Compile-time loop: f(integral_constant<int, I>) for I = B .. E-1.
+template <int B, int E, class F>
+__device__ __forceinline__ void static_for(F &&f)
+{
+    if constexpr (B < E) {
+        f(std::integral_constant<int, B>{});
+        static_for<B + 1, E>(f);
+    }
+}
+
+// One S column (index C, an immediate) set to -inf as a predicated select:
+// past cb; before ca; or outside "C <= cb and (C >= ca or C < cg)".
+template <int C>
+__device__ __forceinline__ void mask_after(uint32_t &v, int cb)
+{
+    asm("{\n\t.reg .pred p;\n\tsetp.lt.s32 p, %1, %2;\n\tselp.b32 %0, 0xFF800000, %0, p;\n\t}"
+        : "+r"(v)
+        : "r"(cb), "n"(C));
+}
+template <int C>
+__device__ __forceinline__ void mask_before(uint32_t &v, int ca)
+{
+    asm("{\n\t.reg .pred p;\n\tsetp.gt.s32 p, %1, %2;\n\tselp.b32 %0, 0xFF800000, %0, p;\n\t}"
+        : "+r"(v)
+        : "r"(ca), "n"(C));
+}
+template <int C>
+__device__ __forceinline__ void mask_general(uint32_t &v, int ca, int cb, int cg)
+{
+    asm("{\n\t.reg .pred a, b;\n\t"
+        "setp.le.s32 b, %3, %4;\n\t"        // C >= cg: not a sink column
+        "setp.gt.and.s32 b, %1, %4, b;\n\t"  // and C < ca: before the band
+        "setp.lt.or.s32 a, %2, %4, b;\n\t"   // or C > cb: past the diagonal
+        "selp.b32 %0, 0xFF800000, %0, a;\n\t}"
+        : "+r"(v)
+        : "r"(ca), "r"(cb), "r"(cg), "n"(C));
+}
+
+// The mask of a partial tile on one row of S (s[4][32], column c = 32 q + e):
+// a key is allowed iff c <= cb and (c >= ca or c < cg).  Nearly always one
+// bound alone decides (the diagonal tile: c <= cb; the tile where the band
+// starts: c >= ca), and those rows test one bound per column.  Every column is
+// a predicated select, never a branch: written as a per-column `if`, tiles
+// where both rules apply measured up to seven times a full tile's softmax.
+__device__ __forceinline__ void mask_cols(uint32_t (&s)[4][32], int ca, int cb, int cg)
+{
+    if (cg >= ca || ca <= 0) {
+        // the sinks (if any) reach the band, or the band covers c >= 0
+        static_for<0, BN>([&](auto ic) {
+            constexpr int c = decltype(ic)::value;
+            mask_after<c>(s[c / 32][c % 32], cb);
+        });
+    } else if (cb >= BN - 1 && cg <= 0) {
+        static_for<0, BN>([&](auto ic) {
+            constexpr int c = decltype(ic)::value;
+            mask_before<c>(s[c / 32][c % 32], ca);
+        });
+    } else {
+        static_for<0, BN>([&](auto ic) {
+            constexpr int c = decltype(ic)::value;
+            mask_general<c>(s[c / 32][c % 32], ca, cb, cg);
+        });
+    }
+}
+
 // Tensor-memory columns are compile-time offsets from the allocated base.
 // One-head kernel: O in [0, HD), two S buffers from S_COL0, two P halves from
 // P_COL0.  Head-pair kernels: O_X at 256x, S_X / P_X at 256x + 128.
@@ -138,7 +203,7 @@ struct PrefillParams {
 // One entry of the tile-walk log per key tile a producer issues: the item's
 // rank, sequence, kv head, unit (head pair, head, or q-tile pair), q tile,
 // residue class, the tile's first key index, and flags (1 full, 2 landmark
-// tile, 4 narrow sink tile).  log[0] counts the entries, log[2..3] holds the
+// tile).  log[0] counts the entries, log[2..3] holds the
 // capacity (a 64-bit count of entries); entry e is at log[WALK_HDR +
 // WALK_ENTRY * e].  The log is a kernel argument of its own, kept out of
 // PrefillParams (a larger parameter block made the control warpgroup spill),
@@ -688,31 +753,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // tiles (k a landmark index): land_lo <= k <= land_hi(i)
                     const int khi = kt.land ? lhi : i, klo = kt.land ? llo : lo;
                     const int kgs = kt.land ? 0 : p.g;
-                    // in tile columns c = k - k0: allowed iff c <= cb and (c >= ca or
-                    // c < cg); one bound alone decides on nearly every partial tile
-                    const int ca = klo - kt.k0, cb = khi - kt.k0, cg = kgs - kt.k0;
-                    if (cg >= ca || ca <= 0) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (q * 32 + e > cb) s[q][e] = __float_as_uint(-INFINITY);
-                    } else if (cb >= BN - 1 && cg <= 0) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (q * 32 + e < ca) s[q][e] = __float_as_uint(-INFINITY);
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                const int c = q * 32 + e;
-                                if (!(c <= cb && (c >= ca || c < cg)))
-                                    s[q][e] = __float_as_uint(-INFINITY);
-                            }
-                    }
+                    // allowed: k <= khi and (k >= klo or k < kgs), in tile columns k - k0
+                    mask_cols(s, klo - kt.k0, khi - kt.k0, kgs - kt.k0);
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -850,20 +892,6 @@ teardown:
 // it through STAGE_WARP bytes of shared memory per warp (store_o_rows_chunked).
 // ------------------------------------------------------------------------
 constexpr int NTHREADS2 = 512;
-// The narrow sink tile: when the sinks 0 .. g-1 (g <= NB_SINK) form a key tile
-// of their own, below the band (every item's first tile then), the pair kernel
-// loads, multiplies and exponentiates only its first NB_SINK keys: S with
-// N = NB_SINK, P V with one K-step of 16 keys.  In the window path the second
-// set of key/value maps (tmK2, tmV2) are boxes of NB_SINK rows for this tile.
-constexpr int NB_SINK = 16;
-// NS: the kernel instantiation that has the narrow sink tile (the window path
-// with 1 <= g <= NB_SINK); the others carry none of its code.
-template <bool PAT, bool NS>
-__device__ __forceinline__ bool narrow_sink_tile(const TileRange &tr, int j, const PrefillParams &p)
-{
-    if constexpr (PAT || !NS) return false;
-    return j == 0 && tr.ns == 1 && p.g <= NB_SINK;
-}
 // named barriers 1 (head A) and 2 (head B): a softmax warpgroup's 128 threads
 // arrive when all of P is in tensor memory, the 32 threads of the MMA warp
 // wait; 3 (A) and 4 (B) likewise when P's first 64 keys are (the pair kernel
@@ -988,7 +1016,7 @@ __device__ __forceinline__ void softmax_half(const uint32_t (&sa)[32], const uin
     }
 }
 
-template <int HD, bool PAT, bool QP, bool NS, bool SKEW, bool WALK>
+template <int HD, bool PAT, bool QP, bool SKEW, bool WALK>
 __global__ void __launch_bounds__(NTHREADS2, 1)
     swa_prefill_bf16_pair_sm103(const __grid_constant__ CUtensorMap tmQ,
                                 const __grid_constant__ CUtensorMap tmK,
@@ -1146,7 +1174,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 // period before S_A(c) needs it, and the MMA warp still waits once per
                 // tile.  The last tile's V rides on the barrier of the tile after it.
                 // pv_*: the previous tile's V, still to be loaded.
-                bool pv_have = false, pv_nar = false;
+                bool pv_have = false;
                 int pv_k0 = 0, pv_kc = 0, pv_z = 0;
                 const CUtensorMap *pv_map = &tmV;
                 // waits until V slot (c_next - 1) % STAGES is free for V(c_next - 1)
@@ -1173,12 +1201,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     const CUtensorMap *mq = (!PAT || cls < p.rem) ? &tmQ : &tmQ2;
                     // the item's Q tiles.  Their buffers free up only at the
                     // previous item's last S, and the MMA warp first needs the
-                    // previous item's last value tile, so on the plain window path
-                    // they go after the item's first key tile (which carries that
-                    // V).  Where the first key tile is the narrow sink tile, and
-                    // for the fixed patterns, they go first: measured 1.5% (sinks)
-                    // and 2-4% (patterns) faster that way, the other order 1-4%
-                    // faster without sinks.
+                    // previous item's last value tile, so on the window path they
+                    // go after the item's first key tile (which carries that V):
+                    // 1-4% faster than the other order.  For the fixed patterns
+                    // they go first: 2-4% faster there.
                     auto load_q_tiles = [&]() -> bool {
                         for (int x = 0; x < 2; ++x) {
                             if (!mbar_wait(BAR(L::Q_EMPTY + x), (it & 1) ^ 1, abort_flag, p.status,
@@ -1194,7 +1220,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         }
                         return true;
                     };
-                    if ((PAT || NS) && !load_q_tiles()) ok = false;
+                    if (PAT && !load_q_tiles()) ok = false;
                     for (int j = 0; ok && j < tr.count; ++j, ++kv_iter) {
                         const int st = kv_iter % STAGES;
                         const uint32_t ph = (kv_iter / STAGES) & 1;
@@ -1217,29 +1243,24 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                             continue;
                         }
                         // this tile's K and the previous tile's V complete this tile's
-                        // barrier.  The narrow sink tile is NB_SINK rows at the top of
-                        // each 64-column chunk (the tmK2/tmV2 boxes).
-                        const bool nar = narrow_sink_tile<PAT, NS>(tr, j, p);
+                        // barrier
                         if constexpr (WALK)
                             log_walk(walk, t, b, kvh, hp, qt, cls, kt.k0,
-                                     (kt.full ? 1 : 0) | (kt.land ? 2 : 0) | (nar ? 4 : 0));
-                        const CUtensorMap *mk = nar ? &tmK2 : hi ? &tmK : &tmK2;
-                        const CUtensorMap *mv = nar ? &tmV2 : hi ? &tmV : &tmV2;
-                        const uint32_t kbytes = nar ? 1u * NB_SINK * HD * 2 : L::KB;
-                        const uint32_t vbytes = !pv_have ? 0u : pv_nar ? 1u * NB_SINK * HD * 2 : L::KB;
-                        mbar_expect_tx(BAR(L::K_FULL + st), kbytes + vbytes);
+                                     (kt.full ? 1 : 0) | (kt.land ? 2 : 0));
+                        const CUtensorMap *mk = hi ? &tmK : &tmK2;
+                        const CUtensorMap *mv = hi ? &tmV : &tmV2;
+                        mbar_expect_tx(BAR(L::K_FULL + st), pv_have ? 2 * L::KB : L::KB);
                         if (pv_have) issue_prev_v(kv_iter, BAR(L::K_FULL + st));
                         for (int c = 0; c < HD / 64; ++c)
                             load_rows<PAT>(sK + st * L::KB + c * (BN * 128), mk, BAR(L::K_FULL + st),
                                            c * 64, kc, kt.k0, zkv);
                         last_k_par[st] = static_cast<int>(ph);
                         pv_have = true;
-                        pv_nar = nar;
                         pv_k0 = kt.k0;
                         pv_kc = kc;
                         pv_z = zkv;
                         pv_map = mv;
-                        if (!PAT && !NS && j == 0 && !load_q_tiles()) {
+                        if (!PAT && j == 0 && !load_q_tiles()) {
                             ok = false;
                             break;
                         }
@@ -1255,7 +1276,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         !mbar_wait(BAR(L::KV_EMPTY + st), ph ^ 1, abort_flag, p.status, p.wait_ns)) {
                         ok = false;
                     } else {
-                        mbar_expect_tx(BAR(L::K_FULL + st), pv_nar ? 1u * NB_SINK * HD * 2 : L::KB);
+                        mbar_expect_tx(BAR(L::K_FULL + st), L::KB);
                         issue_prev_v(kv_iter, BAR(L::K_FULL + st));
                         last_k_par[st] = static_cast<int>(ph);
                     }
@@ -1280,11 +1301,10 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         // group and the K-steps are unrolled with compile-time offsets.
         {
             const uint32_t idesc_s = idesc_bf16_f32(128, BN, 0);
-            const uint32_t idesc_s16 = idesc_bf16_f32(128, NB_SINK, 0);
             const uint32_t idesc_o = idesc_bf16_f32(128, HD, 1);
             int kv_iter = 0, it = 0, c = 0;
             bool ok = true;
-            bool have_prev = false, prev_first = false, prev_last = false, prev_narrow = false;
+            bool have_prev = false, prev_first = false, prev_last = false;
             int prev_st = 0, prev_c = 0, prev_it = 0;
             // P_X(prev) V into O_X
             auto issue_pv = [&](auto xc) -> bool {
@@ -1303,13 +1323,11 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 tc_fence_after();
                 const uint64_t vb = smem_desc_sw128(sV + prev_st * L::KB, BN * 128, 1024);
                 const uint32_t o_t = tmem + x * 256, p_t = tmem + x * 256 + 128;
-                if (!prev_narrow) mma_ts_group4(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
+                mma_ts_group4(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
                 asm volatile("bar.sync %0, %1;" ::"n"(1 + x), "n"(P_BAR_THREADS) : "memory");
                 tc_fence_after();
-                if (prev_narrow)  // the narrow sink tile: one K-step of 16 keys
-                    mma_ts_e(o_t, p_t, vb, idesc_o, prev_first ? 0u : 1u);
-                else  // keys 64..127: P columns 32.., V rows 64.. (64 * 128 B >> 4)
-                    mma_ts_group4(o_t, p_t + 32, vb + 512, idesc_o, 1u);
+                // keys 64..127: P columns 32.., V rows 64.. (64 * 128 B >> 4)
+                mma_ts_group4(o_t, p_t + 32, vb + 512, idesc_o, 1u);
                 // the V slot (window path) or the whole K/V stage (fixed patterns)
                 if (x == 1) tc_commit_e(BAR((SKEW ? L::V_EMPTY : L::KV_EMPTY) + prev_st));
                 if (prev_last) tc_commit_e(BAR(L::O_FULL + x));
@@ -1318,12 +1336,12 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                 return !*abort_flag;
             };
             // S_X = Q_X K^T
-            auto issue_s = [&](auto xc, int st, bool last, bool narrow) {
+            auto issue_s = [&](auto xc, int st, bool last) {
                 constexpr int x = decltype(xc)::value;
                 const uint64_t qb = smem_desc_sw128(sQ + x * L::QB, 16, 1024);
                 const uint64_t kb = smem_desc_sw128(sK + st * L::KB, 16, 1024);
                 const uint32_t s_t = tmem + x * 256 + 128;
-                mma_ss_group<HD / 16>(s_t, qb, kb, narrow ? idesc_s16 : idesc_s);
+                mma_ss_group<HD / 16>(s_t, qb, kb, idesc_s);
                 tc_commit_e(BAR(L::S_FULL + x));
                 if (last) tc_commit_e(BAR(L::Q_EMPTY + x));
                 if (SKEW && x == 1) tc_commit_e(BAR(L::KV_EMPTY + st));  // the K slot
@@ -1332,20 +1350,17 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             using X1 = std::integral_constant<int, 1>;
             for (int t = pair_item_rank(blockIdx.x, 0); ok && t < pairs_per_item_count;
                  t = pair_item_rank(blockIdx.x, ++it)) {
-                // the item's tile count and narrow flag: worked out here on the
-                // skewed path (items of many tiles); for items of one or two
+                // the item's tile count: worked out here on the skewed path
+                // (items of many tiles); for items of one or two
                 // tiles, where the issuer's own index arithmetic showed, taken
                 // from the producer (item_info) once the item's first Q barrier
                 // has passed (measured 4% faster on the strided pattern, no
                 // gain or 1% slower on long items)
                 int count = 1;
-                bool first_narrow = false;
                 if constexpr (SKEW) {
                     int b, hp, kvh, qt, cls, off;
                     decode_level_item<PAT>(t, p, pair_units<QP>(p), b, hp, kvh, qt, cls);
-                    const TileRange tr = item_tiles<PAT, QP>(p, b, qt, cls, off);
-                    count = tr.count;
-                    first_narrow = narrow_sink_tile<PAT, NS>(tr, 0, p);
+                    count = item_tiles<PAT, QP>(p, b, qt, cls, off).count;
                 }
                 for (int j = 0; j < count; ++j, ++kv_iter, ++c) {
                     const int st = kv_iter % STAGES;
@@ -1371,9 +1386,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     }
                     if (!SKEW && j == 0) count = item_info[it & 3];
                     const bool last = (j == count - 1);
-                    const bool narrow = j == 0 && first_narrow;
                     tc_fence_after();
-                    issue_s(X0{}, st, last, narrow);
+                    issue_s(X0{}, st, last);
                     // head B: P_B(c-1) V, then S_B(c)
                     if (have_prev && !issue_pv(X1{})) {
                         ok = false;
@@ -1384,14 +1398,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                         break;
                     }
                     tc_fence_after();
-                    issue_s(X1{}, st, last, narrow);
+                    issue_s(X1{}, st, last);
                     have_prev = true;
                     prev_st = st;
                     prev_c = c;
                     prev_it = it;
                     prev_first = (j == 0);
                     prev_last = last;
-                    prev_narrow = narrow;
                 }
             }
             // the last tile's V (window path: on the barrier of the tile after it)
@@ -1457,39 +1470,6 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     break;
                 }
                 tc_fence_after();
-                if (narrow_sink_tile<PAT, NS>(tr, j, p)) {
-                    // the item's first tile: NB_SINK sink keys (key indices 0 ..),
-                    // masked with the general rule; m starts here
-                    uint32_t sn[NB_SINK];
-                    tmem_ld16(s_addr, sn);
-                    tmem_ld_wait();
-                    reg_fence16(sn);
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < NB_SINK; ++e) {
-                        if (!(e <= i && (e >= lo || e < p.g))) sn[e] = __float_as_uint(-INFINITY);
-                        mx = fmaxf(mx, __uint_as_float(sn[e]));
-                    }
-                    m = mx * sl2;
-                    const float m_use = (m == -INFINITY) ? 0.f : m;
-                    uint32_t pn[NB_SINK / 2];
-                    float ls = 0.f;
-#pragma unroll
-                    for (int e = 0; e < NB_SINK; e += 2) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sn[e]), sl2, -m_use));
-                        const float p1 = ex2(fmaf(__uint_as_float(sn[e + 1]), sl2, -m_use));
-                        ls += p0 + p1;
-                        pn[e >> 1] = pack_bf16x2(p0, p1);
-                    }
-                    l = ls;
-                    tmem_st8(s_addr, pn);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    p_arrive_half(x);
-                    p_arrive(x);
-                    continue;
-                }
                 uint32_t s[4][32];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tmem_ld32(s_addr + q * 32, s[q]);
@@ -1503,34 +1483,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                     // tiles (k a landmark index): land_lo <= k <= land_hi(i)
                     const int khi = kt.land ? lhi : i, klo = kt.land ? llo : lo;
                     const int kgs = kt.land ? 0 : p.g;
-                    // in tile columns c = k - k0: allowed iff c <= cb and (c >= ca or
-                    // c < cg).  Nearly always one bound alone decides (the diagonal
-                    // tile: c <= cb; the tile where the band starts: c >= ca), so
-                    // those rows test one bound per element
-                    const int ca = klo - kt.k0, cb = khi - kt.k0, cg = kgs - kt.k0;
-                    if (cg >= ca || ca <= 0) {
-                        // the sinks (if any) reach the band, or the band covers c >= 0
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (q * 32 + e > cb) s[q][e] = __float_as_uint(-INFINITY);
-                    } else if (cb >= BN - 1 && cg <= 0) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (q * 32 + e < ca) s[q][e] = __float_as_uint(-INFINITY);
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                const int c = q * 32 + e;
-                                if (!(c <= cb && (c >= ca || c < cg)))
-                                    s[q][e] = __float_as_uint(-INFINITY);
-                            }
-                    }
+                    // allowed: k <= khi and (k >= klo or k < kgs), in tile columns k - k0
+                    mask_cols(s, klo - kt.k0, khi - kt.k0, kgs - kt.k0);
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -1862,13 +1816,13 @@ int launch_duo(const CUtensorMap &mq, const CUtensorMap &mkh, const CUtensorMap 
 
 // One launch of the pair kernel: head pairs of an even group, or (QP) pairs of
 // adjacent q tiles of one head for an odd group.
-template <int HD, bool WALK, bool PAT, bool QP, bool NS, bool SKEW = true>
+template <int HD, bool WALK, bool PAT, bool QP, bool SKEW = true>
 int launch_pair(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                 const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
                 PrefillParams p, int per_unit, cudaStream_t stream, int32_t *walk)
 {
     using L2 = Layout2<HD>;
-    if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS, SKEW, WALK>>(L2::DYN_SMEM) !=
+    if (smem_opt_in<swa_prefill_bf16_pair_sm103<HD, PAT, QP, SKEW, WALK>>(L2::DYN_SMEM) !=
         cudaSuccess)
         return SWA_ERR_CUDA;
     if constexpr (QP) {
@@ -1878,7 +1832,7 @@ int launch_pair(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap 
         p.num_items = p.B * p.Hkv * (p.G / 2) * per_unit;
     }
     const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-    swa_prefill_bf16_pair_sm103<HD, PAT, QP, NS, SKEW, WALK>
+    swa_prefill_bf16_pair_sm103<HD, PAT, QP, SKEW, WALK>
         <<<grid, NTHREADS2, L2::DYN_SMEM, stream>>>(mq, mk, mv, mq2, mk2, mv2, p, walk);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
@@ -1888,20 +1842,16 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
                    const CUtensorMap &mq2, const CUtensorMap &mk2, const CUtensorMap &mv2,
                    PrefillParams p, int per_unit, cudaStream_t stream, int32_t *walk)
 {
-    // pair<QP, NS, SKEW>(): one launch of that pair-kernel instantiation
-    auto pair = [&](auto qp, auto ns, auto skew) {
-        return launch_pair<HD, WALK, PAT, decltype(qp)::value, decltype(ns)::value,
-                           decltype(skew)::value>(mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream,
-                                                  walk);
+    // pair<QP, SKEW>(): one launch of that pair-kernel instantiation
+    auto pair = [&](auto qp, auto skew) {
+        return launch_pair<HD, WALK, PAT, decltype(qp)::value, decltype(skew)::value>(
+            mq, mk, mv, mq2, mk2, mv2, p, per_unit, stream, walk);
     };
     using T = std::true_type;
     using F = std::false_type;
     if constexpr (!PAT) {
-        // the window path: the narrow sink tile is compiled in only where it is
-        // used (1 <= g <= NB_SINK); an odd group pairs adjacent q tiles of one head
-        const bool ns = p.g >= 1 && p.g <= NB_SINK;
-        if (p.G % 2 == 0) return ns ? pair(F{}, T{}, T{}) : pair(F{}, F{}, T{});
-        return ns ? pair(T{}, T{}, T{}) : pair(T{}, F{}, T{});
+        // the window path: head pairs; an odd group pairs adjacent q tiles of one head
+        return p.G % 2 == 0 ? pair(F{}, T{}) : pair(T{}, T{});
     } else {
         // the fixed patterns: head pairs for even groups, the single-head kernel
         // for odd ones.  An item's key tiles number about min(window, class
@@ -1910,7 +1860,7 @@ int launch_kernels(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
         // strided head's short classes).
         if (p.G % 2 == 0) {
             const int span = p.w < p.n_hi ? p.w : p.n_hi;
-            return span >= 4 * BN ? pair(F{}, F{}, T{}) : pair(F{}, F{}, F{});
+            return span >= 4 * BN ? pair(F{}, T{}) : pair(F{}, F{});
         }
         using L = Layout<HD>;
         if (smem_opt_in<swa_prefill_bf16_sm103<HD, PAT, WALK>>(L::DYN_SMEM) != cudaSuccess)
@@ -1938,11 +1888,11 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     CUtensorMap mq, mk, mv, mq2, mk2, mv2;
     bool ok;
     if (!pat) {
-        // the second key/value maps are the narrow sink tile's boxes of NB_SINK rows
         ok = make_map_3d(&mq, Q, HD, n, ZQ, BM) && make_map_3d(&mk, K, HD, n_k, ZK, BN) &&
-             make_map_3d(&mv, V, HD, n_k, ZK, BN) && make_map_3d(&mk2, K, HD, n_k, ZK, NB_SINK) &&
-             make_map_3d(&mv2, V, HD, n_k, ZK, NB_SINK);
+             make_map_3d(&mv, V, HD, n_k, ZK, BN);
         mq2 = mq;
+        mk2 = mk;
+        mv2 = mv;
     } else if (rl > 0) {
         // landmarks: Q, K, V as they are, and K, V as the stride-rl view whose
         // class 0 lists positions 0, rl, 2 rl, ... (ceil(n/rl) of them)
@@ -2005,11 +1955,10 @@ int launch_hd(const void *Q, const void *K, const void *V, void *O, float *lse, 
     // per-tile check for it
     // the window path on CTA pairs, on request only (it measured 4-9% slower
     // than the pair kernel on the Mistral-like, Gemma-3-like and long layers):
-    // d = 128, an even group, heads in quads, no narrow sink tile
+    // d = 128, an even group, heads in quads
     if (cta_pairs) {
         if constexpr (HD == 128) {
-            if (!pat && walk == nullptr && p.G % 2 == 0 && H % 4 == 0 &&
-                !(g >= 1 && g <= NB_SINK)) {
+            if (!pat && walk == nullptr && p.G % 2 == 0 && H % 4 == 0) {
                 CUtensorMap mkh;
                 if (!make_map_3d(&mkh, K, HD, n_k, ZK, BN / 2)) return SWA_ERR_CUDA;
                 return p.G % 4 == 0 ? launch_duo<HD, true>(mq, mkh, mv, p, stream)

@@ -19,6 +19,7 @@ CASES = [
     (1, 8, 1, 1000, 128, 1000, 0),  # G = 8, full causal
     (3, 12, 6, 777, 128, 64, 0),    # window narrower than a tile, three sequences
     (1, 4, 1, 1, 128, 1, 0),        # one row, w = 1
+    (1, 8, 2, 1200, 128, 300, 4),   # four sinks in a tile of their own, below the band
 ]
 
 
@@ -61,8 +62,7 @@ def test_cta_pairs_full_size_sampled_rows(swa, oracle_mod, name):
 @pytest.mark.gpu
 @pytest.mark.parametrize("H,Hkv,d,g", [(4, 1, 64, 0),    # d = 64
                                        (3, 1, 128, 0),   # odd group
-                                       (2, 1, 128, 0),   # H % 4 != 0
-                                       (4, 2, 128, 4)])  # the narrow sink tile (g <= 16)
+                                       (2, 1, 128, 0)])  # H % 4 != 0
 def test_cta_pairs_refuses_other_shapes(swa, H, Hkv, d, g):
     x = synthetic.prefill_inputs(1, H, Hkv, 256, d, 64, g, dtype="bf16", seed=0, device="cuda")
     with pytest.raises(swa.SwaError) as e:

@@ -40,11 +40,11 @@ def test_prefill_bf16_matches_oracle(swa, oracle_mod, B, H, Hkv, n, d, w, g):
     assert np.abs(lse.cpu().double().numpy() - L).max() < 2e-3
 
 
-# The narrow sink tile: once the band of a 128-row query tile starts past key
-# tile 0, the sinks 0..g-1 (g <= 16) are read through a 16-key tile.  Shapes
-# with n well past w + 128, so most query tiles take it; g = 16 is the widest
-# narrow tile, g = 17 the narrowest full one; odd groups (q-tile pairs) too.
-NARROW_SINK_CASES = [
+# A sink tile of its own: once the band of a 128-row query tile starts past
+# key tile 0, the sinks 0..g-1 are read through key tile 0, masked to its first
+# g keys.  Shapes with n well past w + 128, so most query tiles take it; a
+# handful of sinks up to 17; odd groups (q-tile pairs) too.
+SINK_TILE_CASES = [
     # B, H, Hkv, n, d, w, g
     (1, 4, 2, 900, 128, 100, 1),
     (2, 2, 1, 1000, 128, 64, 4),
@@ -56,8 +56,8 @@ NARROW_SINK_CASES = [
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("B,H,Hkv,n,d,w,g", NARROW_SINK_CASES)
-def test_prefill_narrow_sink_tile_matches_oracle(swa, oracle_mod, B, H, Hkv, n, d, w, g):
+@pytest.mark.parametrize("B,H,Hkv,n,d,w,g", SINK_TILE_CASES)
+def test_prefill_sink_tile_below_band_matches_oracle(swa, oracle_mod, B, H, Hkv, n, d, w, g):
     x = synthetic.prefill_inputs(B, H, Hkv, n, d, w, g, dtype="bf16", seed=n + g, sink_scale=4.0,
                                  device="cuda")
     lse = torch.empty(B, H, n, dtype=torch.float32, device="cuda")

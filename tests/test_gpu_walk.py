@@ -3,8 +3,7 @@
 oracle defines it: every 128-row query tile of every head is visited by
 exactly one work item, which loads exactly the key tiles holding at least one
 allowed (query, key) pair, sink tiles before band tiles, each once; tiles the
-kernel treats as mask-free are those the oracle finds full; the narrow sink
-tile is taken exactly where it applies.  ("Sliding Window and Sparse
+kernel treats as mask-free are those the oracle finds full.  ("Sliding Window and Sparse
 Attention, from Longformer to CSA2", section 4: block-sparse attention reads
 only the tiles that meet the band; "Local and Sparse Attention: Reading Fewer
 Token Positions", Figures 1-2.)"""
@@ -17,7 +16,7 @@ from sink_sparse_attention_swa_b300 import synthetic
 from tests.parity import assert_close
 
 BM = BN = 128
-FULL, LAND, NARROW = 1, 2, 4
+FULL, LAND = 1, 2
 
 
 def group_items(entries):
@@ -57,17 +56,13 @@ def check_window_walk(items, B, H, Hkv, n, w, g, oracle_mod):
         if pairs:  # mask-free tiles are exactly the oracle's full ones
             for k0, fl in tiles:
                 assert bool(fl & FULL) == (cls[q, k0 // BN] == 2), (q, k0, fl)
-        # the narrow sink tile: tile 0 when it is below the band and 1 <= g <= 16
-        for k0, fl in tiles:
-            q0 = (q if pairs else 2 * q) * BM
-            band_start_tile = max(0, q0 - w + 1) // BN
-            narrow = k0 == 0 and 1 <= g <= 16 and band_start_tile >= 1
-            assert bool(fl & NARROW) == narrow, (q, k0, fl, g)
+        for k0, fl in tiles:  # no flag outside full and landmark
+            assert fl & ~(FULL | LAND) == 0, (q, k0, fl)
 
 
 CASES = [
     # B, H, Hkv, n, d, w, g
-    (2, 4, 2, 700, 128, 200, 4),      # even group, narrow sink tile
+    (2, 4, 2, 700, 128, 200, 4),      # even group, 4 sinks in a tile below the band
     (1, 3, 1, 900, 64, 300, 0),       # group of 3: q-tile pairs
     (1, 2, 1, 600, 128, 100, 20),     # 20 sinks: a full 128-key sink tile
     (1, 2, 2, 1000, 128, 1000, 0),    # multi-head attention, full causal

@@ -4,11 +4,12 @@ swa_prefill_bf16_pair_sm103), run under random schedules.
 The roles are sequential programs that wait on and arrive at barriers in the
 kernel's order:
 
-* the producer.  Window path (skewed protocol): tile c's barrier carries K(c)
-  and V(c-1).  The Q tiles go after the item's first key tile, or before it
-  where the kernel is built for the narrow sink tile.  Fixed patterns: one
-  stage per tile for K and V, the Q tiles first, the item's tile count posted
-  in a four-slot ring;
+* the producer.  Skewed protocol (the window path, and fixed patterns with
+  items of four tiles and more): tile c's barrier carries K(c) and V(c-1).
+  The Q tiles go after the item's first key tile on the window path, first
+  for the patterns.  Fixed patterns with short items: one stage per tile for
+  K and V, the Q tiles first, the item's tile count posted in a four-slot
+  ring;
 * the MMA warp: per tile, P_A(c-1) V in two halves, S_A(c), P_B(c-1) V, S_B(c);
 * the two softmax warpgroups: S read, O rescaled in place, P handed over in two
   halves on hardware named barriers, row statistics posted per item;
@@ -328,8 +329,8 @@ def random_items(rnd, max_tiles):
 # (skewed K/V protocol, Q tiles before the first key tile, tiles per item)
 PROTOCOLS = {
     "window": (True, False, 5),
-    "window_narrow_sink": (True, True, 5),
-    "fixed_pattern": (False, True, 2),
+    "pattern_skewed": (True, True, 5),
+    "pattern_per_tile_stage": (False, True, 2),
 }
 
 
@@ -343,7 +344,7 @@ def test_pair_kernel_protocol_holds_under_random_schedules(name):
 
 @pytest.mark.parametrize("plant,name,expect", [
     ("final_v_unguarded", "window", "armed again"),
-    ("short_info_ring", "fixed_pattern", "tile count"),
+    ("short_info_ring", "pattern_per_tile_stage", "tile count"),
 ])
 def test_model_catches_planted_protocol_mistakes(plant, name, expect):
     skew, q_first, max_tiles = PROTOCOLS[name]
