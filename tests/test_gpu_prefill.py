@@ -23,6 +23,12 @@ BF16_CASES = [
     (1, 16, 1, 300, 128, 100, 2),    # group of 16: eight head pairs per kv head
     (2, 5, 1, 260, 128, 70, 1),      # odd group of 5: single-head kernel
     (2, 32, 16, 384, 128, 128, 0),   # the Gemma-3 head shape, window of one tile
+    # the three mask rules of a partial tile: sinks reaching into the band's first
+    # tile, a window far narrower than a tile beside sinks filling most of one,
+    # and sinks spanning two tiles with a window of 5 (d = 64)
+    (1, 2, 1, 600, 128, 100, 60),
+    (1, 4, 2, 700, 128, 30, 120),
+    (1, 2, 2, 500, 64, 5, 200),
 ]
 
 
