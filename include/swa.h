@@ -211,8 +211,11 @@ int swa_prefill_chunk(const void *Q, const void *k_new, const void *v_new, void 
  * streams may overlap safely.  A workspace grows on demand (cudaMalloc when a
  * stream first needs more, so make the first call of a size on a stream
  * outside stream capture); an outgrown buffer is kept, not freed, until the
- * process exits, because kernels or captured graphs may still use it.  Returns
- * SWA_ERR_ALLOC, enqueuing nothing, if that allocation fails.
+ * process exits, because kernels or captured graphs may still use it.  A
+ * stream's workspace also outlives the stream (the library is not told when a
+ * stream is destroyed): a program that creates many short-lived streams should
+ * call swa_decode_ex with a workspace of its own.  Returns SWA_ERR_ALLOC,
+ * enqueuing nothing, if that allocation fails.
  */
 int swa_decode(const void *q, const void *Kcache, const void *Vcache, const int32_t *pos,
                int B, int H, int Hkv, int d, int w, int g, float scale, void *O,
